@@ -1,0 +1,455 @@
+/*
+ * Barnes-Hut gravity oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU restatement of what the GPU path
+ * computes.  Only the test suite, the smoke check and the benchmark's CPU
+ * baseline may load it; the library never calls it.  It shares no code,
+ * header, table or constant with the CUDA sources.
+ *
+ * Sources (web pages this library implements):
+ *   [T] "GASPHiA中的自引力树代码效率与优化分析" (yekq.top, GASPHiA tree code):
+ *       sections "计算核函数" (the stages: bounding box, build, centre of mass,
+ *       gravity), "性能瓶颈分析" (opening test w_sq/theta_sq < r_sq and the
+ *       warp vote), "排序算法" (spatial sort), "精度与加速比验证" (brute force
+ *       double loop as the accuracy reference).
+ *   [S] "树结构（基于根据 Burtscher 和 Pingali 的研究）" (yekq.top, tree
+ *       neighbour search): sections "实现步骤" (bounding box by reduction,
+ *       Morton / Z-order keys and spatial sort), "构建树结构" (octant number
+ *       x -> +1, y -> +2, z -> +4; subdivide until particles separate).
+ *
+ * Floating point: physics (centres of mass, forces, potentials) in fp64.  The
+ * two integer-valued decisions the GPU takes in fp32 -- the bounding cube and
+ * the Morton quantisation -- are taken here in fp32 with the same IEEE
+ * operations (compile with -ffp-contract=off, no -ffast-math), as the pages
+ * fix single precision for the particle data ([T] "性能测试与对比": 单精度).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - softening: a_i = -G sum m_j (x_i-x_j)/(|x_i-x_j|^2+eps^2)^{3/2},
+ *    phi_i = -G sum m_j/(|x_i-x_j|^2+eps^2)^{1/2}; the pages give G only as a
+ *    parameter and no eps.
+ *  - cube anchored at the per-axis minimum lo with side L = max extent (1 if
+ *    every point coincides); quantise q = trunc((x-lo)*(2^b/L)) clamped to
+ *    [0, 2^b-1] -- a point on a split plane goes to the upper half.
+ *  - w in the opening test is the full cell edge L/2^level; accept a cell iff
+ *    w^2/theta^2 < r^2 (strict), r = distance from the target to the cell's
+ *    centre of mass; the test applies to every cell, leaves included.
+ *  - canonical octree with leaf capacity B: the root is level 0; a cell exists
+ *    iff its parent is internal and some key lies in it; a cell is internal
+ *    iff it holds more than B particles and its level is below b.
+ *  - self mode skips the pair j == i by index; with eps == 0 a pair at zero
+ *    separation contributes nothing.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_EINVAL 1
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bounding cube ([S] 实现步骤 "确定粒子空间范围": min/max by reduction).        */
+/* cube[0..2] = lo, cube[3] = L.  Returns ORC_EINVAL on NaN/Inf input.       */
+/* ------------------------------------------------------------------------ */
+int orc_bbox(const float *pm, int64_t n, float *cube)
+{
+    if (n <= 0) return ORC_EINVAL;
+    float lo[3], hi[3];
+    for (int a = 0; a < 3; ++a) { lo[a] = pm[a]; hi[a] = pm[a]; }
+    for (int64_t i = 0; i < n; ++i) {
+        for (int a = 0; a < 4; ++a)
+            if (!isfinite(pm[4 * i + a])) return ORC_EINVAL;
+        for (int a = 0; a < 3; ++a) {
+            float v = pm[4 * i + a];
+            if (v < lo[a]) lo[a] = v;
+            if (v > hi[a]) hi[a] = v;
+        }
+    }
+    float L = 0.0f;
+    for (int a = 0; a < 3; ++a) {
+        float e = hi[a] - lo[a];            /* fp32 subtraction */
+        if (e > L) L = e;
+    }
+    if (L == 0.0f) L = 1.0f;
+    for (int a = 0; a < 3; ++a) cube[a] = lo[a];
+    cube[3] = L;
+    return ORC_OK;
+}
+
+/* Quantise one coordinate to b bits on the cube (fp32, fixed op order). */
+static uint32_t quantise(float x, float lo, float s, int bits)
+{
+    float v = (x - lo) * s;                 /* fp32 sub, then fp32 mul */
+    float top = (float)((1u << bits) - 1u);
+    if (!(v > 0.0f)) v = 0.0f;              /* also maps NaN (0*inf) to 0 */
+    if (v > top) v = top;
+    return (uint32_t)v;                     /* truncation toward zero */
+}
+
+void orc_quantise(const float *pm, int64_t n, const float *cube, int bits,
+                  uint32_t *q)
+{
+    float s = (float)(1u << bits) / cube[3];   /* IEEE fp32 division */
+    for (int64_t i = 0; i < n; ++i)
+        for (int a = 0; a < 3; ++a)
+            q[3 * i + a] = quantise(pm[4 * i + a], cube[a], s, bits);
+}
+
+/* Z-order interleave: bit k of qx -> key bit 3k, qy -> 3k+1, qz -> 3k+2, so
+ * each 3-bit digit is the octant number x->1, y->2, z->4 of [S] 构建树结构. */
+uint64_t orc_interleave(uint32_t qx, uint32_t qy, uint32_t qz, int bits)
+{
+    uint64_t key = 0;
+    for (int k = 0; k < bits; ++k) {
+        key |= (uint64_t)((qx >> k) & 1u) << (3 * k);
+        key |= (uint64_t)((qy >> k) & 1u) << (3 * k + 1);
+        key |= (uint64_t)((qz >> k) & 1u) << (3 * k + 2);
+    }
+    return key;
+}
+
+void orc_keys(const float *pm, int64_t n, const float *cube, int bits,
+              uint64_t *keys)
+{
+    float s = (float)(1u << bits) / cube[3];
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t qx = quantise(pm[4 * i + 0], cube[0], s, bits);
+        uint32_t qy = quantise(pm[4 * i + 1], cube[1], s, bits);
+        uint32_t qz = quantise(pm[4 * i + 2], cube[2], s, bits);
+        keys[i] = orc_interleave(qx, qy, qz, bits);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Spatial sort ([S] 实现步骤 "粒子空间排序"): stable by key, ties by index.      */
+/* ------------------------------------------------------------------------ */
+typedef struct { uint64_t key; uint32_t idx; } kv_t;
+
+static int kv_cmp(const void *a, const void *b)
+{
+    const kv_t *x = (const kv_t *)a, *y = (const kv_t *)b;
+    if (x->key != y->key) return x->key < y->key ? -1 : 1;
+    return x->idx < y->idx ? -1 : (x->idx > y->idx);
+}
+
+int orc_sort(const uint64_t *keys, int64_t n, uint32_t *perm)
+{
+    kv_t *t = (kv_t *)malloc(sizeof(kv_t) * (size_t)(n > 0 ? n : 1));
+    if (!t) return ORC_EINVAL;
+    for (int64_t i = 0; i < n; ++i) { t[i].key = keys[i]; t[i].idx = (uint32_t)i; }
+    qsort(t, (size_t)n, sizeof(kv_t), kv_cmp);
+    for (int64_t i = 0; i < n; ++i) perm[i] = t[i].idx;
+    free(t);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Canonical octree over sorted keys, breadth first ([S] 构建树结构: a cell is  */
+/* subdivided while it holds too many particles; children in octant order).  */
+/* Node arrays: level, first (sorted index), count, child (index of the first */
+/* child or -1), nchild.  Returns the node count, or -1 if cap is too small.  */
+/* ------------------------------------------------------------------------ */
+static int digit_at(uint64_t key, int level, int bits)
+{
+    /* 3-bit digit selecting the child at `level` (1..bits) */
+    return (int)((key >> (3 * (bits - level))) & 7u);
+}
+
+int64_t orc_build_tree(const uint64_t *skeys, int64_t n, int bits, int leaf_cap,
+                       int64_t cap, int32_t *level, int64_t *first,
+                       int64_t *count, int64_t *child, int32_t *nchild)
+{
+    if (n <= 0) return 0;
+    if (cap < 1) return -1;
+    int64_t head = 0, tail = 0;
+    level[tail] = 0; first[tail] = 0; count[tail] = n;
+    child[tail] = -1; nchild[tail] = 0; ++tail;
+    while (head < tail) {                   /* queue order = breadth first */
+        int64_t c = head++;
+        int l = level[c];
+        if (!(count[c] > leaf_cap && l < bits)) continue;   /* leaf */
+        int64_t s = first[c], e = first[c] + count[c];
+        child[c] = tail;
+        int64_t run = s;
+        while (run < e) {
+            int d = digit_at(skeys[run], l + 1, bits);
+            int64_t r = run;
+            while (r < e && digit_at(skeys[r], l + 1, bits) == d) ++r;
+            if (tail >= cap) return -1;
+            level[tail] = l + 1; first[tail] = run; count[tail] = r - run;
+            child[tail] = -1; nchild[tail] = 0; ++tail;
+            nchild[c] += 1;
+            run = r;
+        }
+    }
+    return tail;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Centre of mass per node ([T] 计算节点质心), fp64 sums over each node's      */
+/* sorted particle range.  A massless node sits at its cell centre.           */
+/* com[4*c..] = (x, y, z, mass).                                              */
+/* ------------------------------------------------------------------------ */
+static uint32_t deinterleave(uint64_t key, int axis, int bits)
+{
+    uint32_t q = 0;
+    for (int k = 0; k < bits; ++k)
+        q |= (uint32_t)((key >> (3 * k + axis)) & 1u) << k;
+    return q;
+}
+
+void orc_com(const float *spm, const uint64_t *skeys, int64_t nnodes,
+             const int32_t *level, const int64_t *first, const int64_t *count,
+             const float *cube, int bits, double *com)
+{
+    double L = cube[3];
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t c = 0; c < nnodes; ++c) {
+        double m = 0.0, sx = 0.0, sy = 0.0, sz = 0.0;
+        for (int64_t j = first[c]; j < first[c] + count[c]; ++j) {
+            double mj = spm[4 * j + 3];
+            m += mj;
+            sx += mj * (double)spm[4 * j + 0];
+            sy += mj * (double)spm[4 * j + 1];
+            sz += mj * (double)spm[4 * j + 2];
+        }
+        if (m != 0.0) {
+            com[4 * c + 0] = sx / m; com[4 * c + 1] = sy / m; com[4 * c + 2] = sz / m;
+        } else {
+            double w = ldexp(L, -level[c]);
+            int sh = bits - level[c];
+            for (int a = 0; a < 3; ++a) {
+                uint32_t cell = deinterleave(skeys[first[c]], a, bits) >> sh;
+                com[4 * c + a] = (double)cube[a] + ((double)cell + 0.5) * w;
+            }
+        }
+        com[4 * c + 3] = m;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* One softened pair term, source (sx,sy,sz,m) acting on target x.           */
+/* ------------------------------------------------------------------------ */
+static inline void pair_term(const double *x, double sx, double sy, double sz,
+                             double m, double eps2, double *acc)
+{
+    double dx = sx - x[0], dy = sy - x[1], dz = sz - x[2];
+    double r2 = dx * dx + dy * dy + dz * dz + eps2;
+    if (r2 == 0.0) return;                  /* eps == 0 and coincident */
+    double inv = 1.0 / sqrt(r2);
+    double inv3 = inv * inv * inv;
+    acc[0] += m * dx * inv3;
+    acc[1] += m * dy * inv3;
+    acc[2] += m * dz * inv3;
+    acc[3] -= m * inv;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Brute-force double loop ([T] 精度与加速比验证: 暴力计算 reference).           */
+/* tgt == NULL: self mode over the sources (pair j == i skipped).            */
+/* idx (may be NULL): evaluate only targets idx[0..k-1]; out has k rows.     */
+/* ------------------------------------------------------------------------ */
+void orc_direct(const float *src, int64_t n, const float *tgt, int64_t m,
+                const int64_t *idx, int64_t k, double G, double eps,
+                double *out)
+{
+    int self = (tgt == NULL);
+    const float *T = self ? src : tgt;
+    int64_t cnt = idx ? k : (self ? n : m);
+    double eps2 = eps * eps;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < cnt; ++r) {
+        int64_t i = idx ? idx[r] : r;
+        double x[3] = {T[4 * i], T[4 * i + 1], T[4 * i + 2]};
+        double acc[4] = {0, 0, 0, 0};
+        for (int64_t j = 0; j < n; ++j) {
+            if (self && j == i) continue;
+            pair_term(x, src[4 * j], src[4 * j + 1], src[4 * j + 2],
+                      src[4 * j + 3], eps2, acc);
+        }
+        for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[a];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Barnes-Hut walk for one target ([T] 性能瓶颈分析: accept a cell iff          */
+/* w_sq/theta_sq < r_sq, otherwise open it; particles are always exact).      */
+/* self_j: sorted index of the target's own particle, or -1.                 */
+/* Returns the number of terms (accepted cells + particle pairs).            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const float *spm;        /* sorted sources (x,y,z,m) */
+    int64_t nnodes;
+    const int32_t *level;
+    const int64_t *first, *count, *child;
+    const int32_t *nchild;
+    const double *com;       /* (x,y,z,m) per node */
+    double L, theta, eps2;
+} tree_t;
+
+static int64_t walk_one(const tree_t *t, const double *x, int64_t self_j,
+                        double *acc, int64_t *stack)
+{
+    double th2 = t->theta * t->theta;
+    int64_t terms = 0, sp = 0;
+    stack[sp++] = 0;
+    while (sp > 0) {
+        int64_t c = stack[--sp];
+        double w = ldexp(t->L, -t->level[c]);
+        const double *cm = t->com + 4 * c;
+        double dx = cm[0] - x[0], dy = cm[1] - x[1], dz = cm[2] - x[2];
+        double r2 = dx * dx + dy * dy + dz * dz;
+        if ((w * w) / th2 < r2) {           /* accept the cell as one mass */
+            pair_term(x, cm[0], cm[1], cm[2], cm[3], t->eps2, acc);
+            ++terms;
+        } else if (t->child[c] < 0) {       /* leaf: its particles, exactly */
+            for (int64_t j = t->first[c]; j < t->first[c] + t->count[c]; ++j) {
+                if (j == self_j) continue;
+                const float *p = t->spm + 4 * j;
+                pair_term(x, p[0], p[1], p[2], p[3], t->eps2, acc);
+                ++terms;
+            }
+        } else {                            /* open: visit children in order */
+            for (int k = t->nchild[c] - 1; k >= 0; --k)
+                stack[sp++] = t->child[c] + k;
+        }
+    }
+    return terms;
+}
+
+/* Per-target Barnes-Hut.  tgt_pos: k target points (x,y,z,*) as fp32 rows;
+ * self_j: k sorted self indices or NULL.  out: k rows (ax,ay,az,phi)*G. */
+void orc_bh(const float *spm, int64_t nnodes, const int32_t *level,
+            const int64_t *first, const int64_t *count, const int64_t *child,
+            const int32_t *nchild, const double *com, double L, double theta,
+            double G, double eps, const float *tgt_pos, const int64_t *self_j,
+            int64_t k, double *out, int64_t *terms)
+{
+    tree_t t = {spm, nnodes, level, first, count, child, nchild, com, L, theta,
+                eps * eps};
+#pragma omp parallel
+    {
+        int64_t *stack = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nnodes + 8));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < k; ++r) {
+            double x[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
+            double acc[4] = {0, 0, 0, 0};
+            int64_t nt = walk_one(&t, x, self_j ? self_j[r] : -1, acc, stack);
+            for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[a];
+            if (terms) terms[r] = nt;
+        }
+        free(stack);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Group walk: the warp-vote form of [T] 性能瓶颈分析.  A group of consecutive */
+/* targets walks the tree together; a cell is accepted only if the test      */
+/* holds for every target of the group (mode 0: per-target vote, the page's  */
+/* __all_sync), or if it holds for the distance from the centre of mass to   */
+/* the group's bounding box (mode 1: box test, which implies mode 0).        */
+/* Every accepted cell and every particle of an opened leaf is applied to    */
+/* every target of the group.  Targets are given in group order.             */
+/* ------------------------------------------------------------------------ */
+void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
+                  const int64_t *first, const int64_t *count,
+                  const int64_t *child, const int32_t *nchild,
+                  const double *com, double L, double theta, double G,
+                  double eps, const float *tgt_pos, const int64_t *self_j,
+                  int64_t k, int64_t group, int mode, double *out,
+                  int64_t *terms)
+{
+    double th2 = theta * theta, eps2 = eps * eps;
+    int64_t ngroups = (k + group - 1) / group;
+#pragma omp parallel
+    {
+        int64_t *stack = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nnodes + 8));
+        double *acc = (double *)malloc(sizeof(double) * 4 * (size_t)group);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t g = 0; g < ngroups; ++g) {
+            int64_t t0 = g * group, t1 = t0 + group < k ? t0 + group : k;
+            double blo[3] = {INFINITY, INFINITY, INFINITY};
+            double bhi[3] = {-INFINITY, -INFINITY, -INFINITY};
+            for (int64_t r = t0; r < t1; ++r)
+                for (int a = 0; a < 3; ++a) {
+                    double v = tgt_pos[4 * r + a];
+                    if (v < blo[a]) blo[a] = v;
+                    if (v > bhi[a]) bhi[a] = v;
+                }
+            memset(acc, 0, sizeof(double) * 4 * (size_t)group);
+            int64_t nterm = 0, sp = 0;
+            stack[sp++] = 0;
+            while (sp > 0) {
+                int64_t c = stack[--sp];
+                double w = ldexp(L, -level[c]);
+                double ropen2 = (w * w) / th2;
+                const double *cm = com + 4 * c;
+                int accept = 1;
+                if (mode == 0) {
+                    for (int64_t r = t0; r < t1 && accept; ++r) {
+                        double dx = cm[0] - tgt_pos[4 * r];
+                        double dy = cm[1] - tgt_pos[4 * r + 1];
+                        double dz = cm[2] - tgt_pos[4 * r + 2];
+                        if (!(ropen2 < dx * dx + dy * dy + dz * dz)) accept = 0;
+                    }
+                } else {
+                    double d2 = 0.0;
+                    for (int a = 0; a < 3; ++a) {
+                        double d = 0.0;
+                        if (cm[a] < blo[a]) d = blo[a] - cm[a];
+                        else if (cm[a] > bhi[a]) d = cm[a] - bhi[a];
+                        d2 += d * d;
+                    }
+                    accept = ropen2 < d2;
+                }
+                if (accept) {
+                    for (int64_t r = t0; r < t1; ++r) {
+                        double x[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
+                        pair_term(x, cm[0], cm[1], cm[2], cm[3], eps2, acc + 4 * (r - t0));
+                    }
+                    nterm += t1 - t0;
+                } else if (child[c] < 0) {
+                    for (int64_t j = first[c]; j < first[c] + count[c]; ++j) {
+                        const float *p = spm + 4 * j;
+                        for (int64_t r = t0; r < t1; ++r) {
+                            if (self_j && self_j[r] == j) continue;
+                            double x[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
+                            pair_term(x, p[0], p[1], p[2], p[3], eps2, acc + 4 * (r - t0));
+                        }
+                    }
+                    nterm += count[c] * (t1 - t0);
+                } else {
+                    for (int q = nchild[c] - 1; q >= 0; --q)
+                        stack[sp++] = child[c] + q;
+                }
+            }
+            for (int64_t r = t0; r < t1; ++r)
+                for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[4 * (r - t0) + a];
+            if (terms) terms[g] = nterm;
+        }
+        free(acc);
+        free(stack);
+    }
+}
