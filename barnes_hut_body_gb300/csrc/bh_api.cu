@@ -1,0 +1,603 @@
+// C ABI of the Barnes-Hut library: context, scratch management and the
+// per-call orchestration of the GPU stages.  No physics here; every step of
+// the path runs in the kernels of k_keys_sort.cu, k_build.cu, k_walk.cu and
+// k_direct.cu.
+//
+// The stage order is the GASPHiA tree-code page's (section "计算核函数":
+// computeBoundingBox -> buildTree -> computeCenterOfMass -> computeGravity),
+// with the spatial sort of the tree page's "实现步骤" section in front of the
+// build.  Unlike the page (a host synchronisation and error check after
+// every stage), the whole call is enqueued on one stream with no host
+// synchronisation, so it can be captured in a CUDA graph; kernels report
+// failures through a device status word read by bh_sync_status.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+#include <vector>
+
+#include "bh_internal.h"
+
+using namespace bh;
+
+struct bh_ctx {
+  int device = 0;
+  int num_sms = 1;
+  float theta = 0.5f, G = 1.f, eps = 0.f;
+  int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
+  unsigned spin_limit = 1u << 22;
+  std::string err;
+
+  DevCtrl *ctrl = nullptr;
+  float4 *partials = nullptr;
+  int bbox_blocks = 0;
+
+  long long cap_n = 0, cap_m = 0, cap_nodes = 0;
+  int cap_tiles_sort = 0, cap_tiles_build = 0;
+  SortBufs sort{}, sort_t{};
+  unsigned long long *status = nullptr;
+  float4 *spm = nullptr, *stm = nullptr;
+  BuildBufs build{};
+
+  double *dpartial = nullptr;
+  long long dpartial_cap = 0;
+
+  float4 *stage_in = nullptr, *stage_tgt = nullptr, *stage_out = nullptr;
+  long long stage_n = 0, stage_m = 0, stage_o = 0;
+
+  cudaEvent_t ev[BH_NUM_STAGES + 1] = {};
+  bool stage_ran[BH_NUM_STAGES] = {};
+  bool timed = false;
+
+  WalkArgs last_walk{};
+  long long last_n = 0, last_m = 0;
+  int last_fb = 0, last_fbt = 0;
+  bool last_self = true, last_valid = false;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+      cudaSetDevice(prev);
+  }
+};
+
+int fail(bh_ctx *c, int code, const std::string &msg) {
+  if (c) c->err = msg;
+  return code;
+}
+
+int cuda_fail(bh_ctx *c, cudaError_t e, const char *where) {
+  return fail(c, BH_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+template <typename T>
+void free_dev(T *&p) {
+  if (p) cudaFree(p);
+  p = nullptr;
+}
+
+template <typename T>
+bool alloc_dev(T *&p, long long count) {
+  free_dev(p);
+  if (count <= 0) count = 1;
+  return cudaMalloc((void **)&p, sizeof(T) * (size_t)count) == cudaSuccess;
+}
+
+long long node_bound(long long n, int leaf_cap, int bits) {
+  // leaves <= n; nodes with >= 2 children < leaves; single-child internal
+  // cells hold > leaf_cap particles and are disjoint within each level below
+  // `bits`, so at most n/(leaf_cap+1) of them per level.
+  return 2 * n + (long long)bits * (n / (leaf_cap + 1) + 1) + 8;
+}
+
+void free_sources(bh_ctx *c) {
+  for (int k = 0; k < 2; ++k) { free_dev(c->sort.keys[k]); free_dev(c->sort.idx[k]); }
+  free_dev(c->spm);
+  free_dev(c->build.topo); free_dev(c->build.parent); free_dev(c->build.level);
+  free_dev(c->build.arrive); free_dev(c->build.msum); free_dev(c->build.rec);
+  free_dev(c->build.tile_counts);
+  c->cap_n = 0; c->cap_nodes = 0;
+}
+
+void free_targets(bh_ctx *c) {
+  for (int k = 0; k < 2; ++k) { free_dev(c->sort_t.keys[k]); free_dev(c->sort_t.idx[k]); }
+  free_dev(c->stm);
+  c->cap_m = 0;
+}
+
+int ensure_status(bh_ctx *c, long long n) {
+  long long tiles = (n + kSortTile - 1) / kSortTile;
+  if (tiles <= c->cap_tiles_sort && c->status) return BH_OK;
+  long long want = tiles + tiles / 4 + 1;
+  if (!alloc_dev(c->status, want * 256)) return fail(c, BH_ENOMEM, "look-back slots");
+  // the tag in every slot must not match a live call: start from zero and
+  // the epoch (which starts at 1 after the first bbox) never tags zero slots
+  cudaMemset(c->status, 0, sizeof(unsigned long long) * (size_t)want * 256);
+  c->cap_tiles_sort = (int)want;
+  c->sort.status = c->sort_t.status = c->status;
+  c->sort.cap_tiles = c->sort_t.cap_tiles = (int)want;
+  return BH_OK;
+}
+
+int ensure_sources(bh_ctx *c, long long n) {
+  const long long need_nodes = node_bound(n, c->leaf_cap, c->bits);
+  if (n <= c->cap_n && need_nodes <= c->cap_nodes) return ensure_status(c, n);
+  cudaDeviceSynchronize();
+  free_sources(c);
+  long long cap = n + n / 8 + 1024;
+  long long nodes = node_bound(cap, c->leaf_cap, c->bits);
+  if (nodes > (1LL << 31) - 1) return fail(c, BH_EINVAL, "too many particles for int32 node indices");
+  bool ok = true;
+  for (int k = 0; k < 2; ++k) {
+    ok = ok && alloc_dev(c->sort.keys[k], cap);
+    ok = ok && alloc_dev(c->sort.idx[k], cap);
+  }
+  ok = ok && alloc_dev(c->spm, cap);
+  ok = ok && alloc_dev(c->build.topo, nodes);
+  ok = ok && alloc_dev(c->build.parent, nodes);
+  ok = ok && alloc_dev(c->build.level, nodes);
+  ok = ok && alloc_dev(c->build.arrive, nodes);
+  ok = ok && alloc_dev(c->build.msum, nodes);
+  ok = ok && alloc_dev(c->build.rec, nodes);
+  long long btiles = (cap + 1 + kBuildTile - 1) / kBuildTile;
+  ok = ok && alloc_dev(c->build.tile_counts, btiles * kMaxLevels);
+  if (!ok) {
+    free_sources(c);
+    return fail(c, BH_ENOMEM, "source scratch allocation failed");
+  }
+  c->cap_n = cap;
+  c->cap_nodes = nodes;
+  c->build.cap_nodes = nodes;
+  c->build.cap_tiles = (int)btiles;
+  return ensure_status(c, cap);
+}
+
+int ensure_targets(bh_ctx *c, long long m) {
+  if (m <= c->cap_m) return ensure_status(c, m);
+  cudaDeviceSynchronize();
+  free_targets(c);
+  long long cap = m + m / 8 + 1024;
+  bool ok = true;
+  for (int k = 0; k < 2; ++k) {
+    ok = ok && alloc_dev(c->sort_t.keys[k], cap);
+    ok = ok && alloc_dev(c->sort_t.idx[k], cap);
+  }
+  ok = ok && alloc_dev(c->stm, cap);
+  if (!ok) {
+    free_targets(c);
+    return fail(c, BH_ENOMEM, "target scratch allocation failed");
+  }
+  c->cap_m = cap;
+  return ensure_status(c, cap);
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_rows(bh_ctx *c, const float *p, size_t rows, const char *name) {
+  if (rows == 0) return BH_OK;
+  if (!p) return fail(c, BH_EINVAL, std::string(name) + " is NULL");
+  if (!aligned16(p)) return fail(c, BH_EINVAL, std::string(name) + " is not 16-byte aligned");
+  if (rows > (size_t)(1LL << 30)) return fail(c, BH_EINVAL, std::string(name) + " has too many rows");
+  return BH_OK;
+}
+
+void record(bh_ctx *c, int i, cudaStream_t s) {
+  if (c->timing) cudaEventRecord(c->ev[i], s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bh_create(bh_ctx **out, int device, size_t max_sources, size_t max_targets) {
+  if (!out) return BH_EINVAL;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+    return BH_EINVAL;
+  bh_ctx *c = new (std::nothrow) bh_ctx();
+  if (!c) return BH_ENOMEM;
+  c->device = device;
+  DeviceGuard g(device);
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (c->num_sms < 1) c->num_sms = 1;
+  c->bbox_blocks = c->num_sms * 4;
+  bool ok = alloc_dev(c->ctrl, 1) && alloc_dev(c->partials, 2LL * c->bbox_blocks);
+  if (ok) ok = cudaMemset(c->ctrl, 0, sizeof(DevCtrl)) == cudaSuccess;
+  for (int i = 0; ok && i <= BH_NUM_STAGES; ++i)
+    ok = cudaEventCreate(&c->ev[i]) == cudaSuccess;
+  if (ok && max_sources) ok = ensure_sources(c, (long long)max_sources) == BH_OK;
+  if (ok && max_targets) ok = ensure_targets(c, (long long)max_targets) == BH_OK;
+  if (ok) ok = ensure_status(c, 1) == BH_OK;
+  if (!ok) {
+    bh_destroy(c);
+    return BH_ENOMEM;
+  }
+  *out = c;
+  return BH_OK;
+}
+
+int bh_destroy(bh_ctx *c) {
+  if (!c) return BH_OK;
+  {
+    DeviceGuard g(c->device);
+    cudaDeviceSynchronize();
+    free_sources(c);
+    free_targets(c);
+    free_dev(c->status);
+    free_dev(c->ctrl);
+    free_dev(c->partials);
+    free_dev(c->dpartial);
+    free_dev(c->stage_in);
+    free_dev(c->stage_tgt);
+    free_dev(c->stage_out);
+    for (int i = 0; i <= BH_NUM_STAGES; ++i)
+      if (c->ev[i]) cudaEventDestroy(c->ev[i]);
+  }
+  delete c;
+  return BH_OK;
+}
+
+int bh_set_params(bh_ctx *c, float theta, float G, float eps) {
+  if (!c) return BH_EINVAL;
+  if (!(theta >= 0.f) || !isfinite(theta)) return fail(c, BH_EINVAL, "theta must be finite and >= 0");
+  if (!isfinite(G)) return fail(c, BH_EINVAL, "G must be finite");
+  if (!(eps >= 0.f) || !isfinite(eps)) return fail(c, BH_EINVAL, "eps must be finite and >= 0");
+  c->theta = theta;
+  c->G = G;
+  c->eps = eps;
+  return BH_OK;
+}
+
+int bh_set_option(bh_ctx *c, int key, long long v) {
+  if (!c) return BH_EINVAL;
+  switch (key) {
+    case BH_OPT_KEY_BITS:
+      if (v != 21 && v != 10) return fail(c, BH_EINVAL, "key bits must be 21 or 10");
+      c->bits = (int)v;
+      return BH_OK;
+    case BH_OPT_LEAF_CAP:
+      if (v < 1 || v > kMaxLeafCap) return fail(c, BH_EINVAL, "leaf capacity must be in 1..64");
+      c->leaf_cap = (int)v;
+      return BH_OK;
+    case BH_OPT_OPENING:
+      if (v != BH_OPEN_VOTE && v != BH_OPEN_BOX) return fail(c, BH_EINVAL, "unknown opening rule");
+      c->opening = (int)v;
+      return BH_OK;
+    case BH_OPT_TIMING:
+      c->timing = v ? 1 : 0;
+      return BH_OK;
+    case BH_OPT_GROUP:
+      if (v != 32 && v != 64) return fail(c, BH_EINVAL, "group must be 32 or 64");
+      c->group = (int)v;
+      return BH_OK;
+    default:
+      return fail(c, BH_EINVAL, "unknown option");
+  }
+}
+
+int bh_set_debug(bh_ctx *c, int key, long long v) {
+  if (!c) return BH_EINVAL;
+  if (key == BH_DBG_SPIN_LIMIT) {
+    if (v < 0 || v > (1LL << 30)) return fail(c, BH_EINVAL, "spin limit out of range");
+    c->spin_limit = (unsigned)v;
+    return BH_OK;
+  }
+  return fail(c, BH_EINVAL, "unknown debug key");
+}
+
+int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
+               size_t m, float *acc_pot, void *stream) {
+  if (!c) return BH_EINVAL;
+  c->err.clear();
+  const bool self = targets == nullptr;
+  const long long N = (long long)n, M = self ? N : (long long)m;
+  int rc;
+  if ((rc = check_rows(c, pos_mass, n, "pos_mass")) != BH_OK) return rc;
+  if (!self && (rc = check_rows(c, targets, m, "targets")) != BH_OK) return rc;
+  if ((rc = check_rows(c, acc_pot, (size_t)M, "acc_pot")) != BH_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceGuard g(c->device);
+  c->last_valid = false;
+  if (M == 0) return BH_OK;
+  if (N == 0) {
+    cudaError_t e = cudaMemsetAsync(acc_pot, 0, sizeof(float4) * (size_t)M, s);
+    return e == cudaSuccess ? BH_OK : cuda_fail(c, e, "memset");
+  }
+  if ((rc = ensure_sources(c, N)) != BH_OK) return rc;
+  if (!self && (rc = ensure_targets(c, M)) != BH_OK) return rc;
+
+  const float4 *pm = reinterpret_cast<const float4 *>(pos_mass);
+  const float4 *tg = reinterpret_cast<const float4 *>(targets);
+  float4 *out = reinterpret_cast<float4 *>(acc_pot);
+  for (int i = 0; i < BH_NUM_STAGES; ++i) c->stage_ran[i] = false;
+
+  cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "memset");
+  record(c, 0, s);
+  int fb = 0, fbt = 0;
+  e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
+  record(c, 1, s);
+  if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
+  record(c, 2, s);
+  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
+  record(c, 3, s);
+  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
+  record(c, 4, s);
+  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
+  record(c, 5, s);
+  if (e == cudaSuccess) e = launch_com(c->spm, c->sort.keys[fb], N, c->bits, c->theta, c->build, c->ctrl, s);
+  record(c, 6, s);
+  if (!self) {
+    if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->bits, false, s);
+    if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->bits, s);
+    if (e == cudaSuccess) e = launch_sort(c->sort_t, M, c->bits, c->ctrl, 1, c->spin_limit, &fbt, s);
+    if (e == cudaSuccess) e = launch_gather(tg, c->sort_t.idx[fbt], M, c->stm, s);
+  }
+  record(c, 7, s);
+  if (e == cudaSuccess) {
+    WalkArgs a;
+    a.spm = c->spm;
+    a.n = N;
+    a.rec = c->build.rec;
+    a.tpos = self ? c->spm : c->stm;
+    a.tperm = self ? c->sort.idx[fb] : c->sort_t.idx[fbt];
+    a.m = M;
+    a.out = out;
+    a.eps2 = c->eps * c->eps;
+    a.G = c->G;
+    a.self_mode = self ? 1 : 0;
+    a.opening = c->opening;
+    a.group = c->group;
+    a.num_sms = c->num_sms;
+    e = launch_walk(a, c->ctrl, s);
+    c->last_walk = a;
+  }
+  record(c, 8, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "launch");
+  for (int i = 0; i < BH_NUM_STAGES; ++i) c->stage_ran[i] = true;
+  c->stage_ran[BH_STAGE_TARGETS] = !self;
+  c->timed = c->timing != 0;
+  c->last_n = N;
+  c->last_m = M;
+  c->last_fb = fb;
+  c->last_fbt = fbt;
+  c->last_self = self;
+  c->last_valid = true;
+  return BH_OK;
+}
+
+int bh_sync_status(bh_ctx *c, void *stream) {
+  if (!c) return BH_EINVAL;
+  DeviceGuard g(c->device);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "stream synchronize");
+  unsigned err = 0;
+  e = cudaMemcpy(&err, &c->ctrl->keep.err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "status read");
+  if (err) {
+    cudaMemset(&c->ctrl->keep.err, 0, sizeof(unsigned));
+    const char *what = err == BH_EINVAL ? "non-finite input"
+                       : err == BH_ETIMEOUT ? "a device wait timed out"
+                       : err == BH_ETREE_OVERFLOW ? "node pool or walk stack overflow"
+                                                  : "device error";
+    return fail(c, (int)err, what);
+  }
+  return BH_OK;
+}
+
+int bh_compute_host(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
+                    size_t m, float *acc_pot, void *stream) {
+  if (!c) return BH_EINVAL;
+  const bool self = targets == nullptr;
+  const long long N = (long long)n, M = self ? N : (long long)m;
+  if (N > 0 && !pos_mass) return fail(c, BH_EINVAL, "pos_mass is NULL");
+  if (M > 0 && !acc_pot) return fail(c, BH_EINVAL, "acc_pot is NULL");
+  if (!self && M > 0 && !targets) return fail(c, BH_EINVAL, "targets is NULL");
+  DeviceGuard g(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (N > c->stage_n) {
+    cudaDeviceSynchronize();
+    if (!alloc_dev(c->stage_in, N + N / 8 + 64)) return fail(c, BH_ENOMEM, "staging");
+    c->stage_n = N + N / 8 + 64;
+  }
+  if (!self && M > c->stage_m) {
+    cudaDeviceSynchronize();
+    if (!alloc_dev(c->stage_tgt, M + M / 8 + 64)) return fail(c, BH_ENOMEM, "staging");
+    c->stage_m = M + M / 8 + 64;
+  }
+  if (M > c->stage_o) {
+    cudaDeviceSynchronize();
+    if (!alloc_dev(c->stage_out, M + M / 8 + 64)) return fail(c, BH_ENOMEM, "staging");
+    c->stage_o = M + M / 8 + 64;
+  }
+  cudaError_t e = cudaSuccess;
+  if (N > 0) e = cudaMemcpyAsync(c->stage_in, pos_mass, sizeof(float4) * (size_t)N, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !self && M > 0)
+    e = cudaMemcpyAsync(c->stage_tgt, targets, sizeof(float4) * (size_t)M, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "host to device copy");
+  int rc = bh_compute(c, (const float *)c->stage_in, n,
+                      self ? nullptr : (const float *)c->stage_tgt, m,
+                      (float *)c->stage_out, stream);
+  if (rc != BH_OK) return rc;
+  if (M > 0) {
+    e = cudaMemcpyAsync(acc_pot, c->stage_out, sizeof(float4) * (size_t)M, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "device to host copy");
+  }
+  return bh_sync_status(c, stream);
+}
+
+int bh_direct(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
+              size_t m, float *acc_pot, void *stream) {
+  if (!c) return BH_EINVAL;
+  c->err.clear();
+  const bool self = targets == nullptr;
+  const long long N = (long long)n, M = self ? N : (long long)m;
+  int rc;
+  if ((rc = check_rows(c, pos_mass, n, "pos_mass")) != BH_OK) return rc;
+  if (!self && (rc = check_rows(c, targets, m, "targets")) != BH_OK) return rc;
+  if ((rc = check_rows(c, acc_pot, (size_t)M, "acc_pot")) != BH_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceGuard g(c->device);
+  if (M == 0) return BH_OK;
+  if (N == 0) {
+    cudaError_t e = cudaMemsetAsync(acc_pot, 0, sizeof(float4) * (size_t)M, s);
+    return e == cudaSuccess ? BH_OK : cuda_fail(c, e, "memset");
+  }
+  long long want = 4 * M * 64;
+  if (want > (1LL << 25)) want = 4 * M > (1LL << 25) ? 4 * M : (1LL << 25);
+  if (c->dpartial_cap < 4 * M) {
+    cudaDeviceSynchronize();
+    if (!alloc_dev(c->dpartial, want)) {
+      c->dpartial_cap = 0;
+      return fail(c, BH_ENOMEM, "direct-sum partials");
+    }
+    c->dpartial_cap = want;
+  }
+  cudaError_t e = launch_direct(reinterpret_cast<const float4 *>(pos_mass), N,
+                                reinterpret_cast<const float4 *>(self ? pos_mass : targets),
+                                M, self, c->eps, c->G, c->dpartial, c->dpartial_cap,
+                                reinterpret_cast<float4 *>(acc_pot), c->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "direct launch");
+  return BH_OK;
+}
+
+int bh_get_stage_times(bh_ctx *c, float *ms, int n) {
+  if (!c || !ms || n < 0 || n > BH_NUM_STAGES) return BH_EINVAL;
+  if (!c->timed) return fail(c, BH_EINVAL, "no timed call (set BH_OPT_TIMING)");
+  DeviceGuard g(c->device);
+  cudaError_t e = cudaEventSynchronize(c->ev[BH_NUM_STAGES]);
+  if (e != cudaSuccess) return cuda_fail(c, e, "event synchronize");
+  for (int i = 0; i < n; ++i) {
+    float t = 0.f;
+    if (c->stage_ran[i]) cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]);
+    ms[i] = t;
+  }
+  return BH_OK;
+}
+
+int bh_get_counters(bh_ctx *c, unsigned long long *executed, unsigned long long *groups) {
+  if (!c) return BH_EINVAL;
+  DeviceGuard g(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(c, e, "synchronize");
+  StepCtrl st;
+  e = cudaMemcpy(&st, &c->ctrl->step, sizeof(StepCtrl), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "counter read");
+  if (executed) *executed = st.executed;
+  if (groups) *groups = st.groups;
+  return BH_OK;
+}
+
+int bh_debug_export(bh_ctx *c, int what, void *dst, size_t bytes) {
+  if (!c || !dst) return BH_EINVAL;
+  if (!c->last_valid) return fail(c, BH_EINVAL, "no completed bh_compute to export");
+  DeviceGuard g(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(c, e, "synchronize");
+  StepCtrl st;
+  e = cudaMemcpy(&st, &c->ctrl->step, sizeof(StepCtrl), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "control read");
+  long long nodes = 0;
+  for (int l = 0; l <= c->bits; ++l) nodes += st.level_total[l];
+  if (nodes > c->cap_nodes) nodes = c->cap_nodes;
+  auto need = [&](size_t b) { return bytes >= b; };
+  switch (what) {
+    case BH_EXPORT_CUBE: {
+      if (!need(16)) return fail(c, BH_EINVAL, "buffer too small");
+      e = cudaMemcpy(dst, &c->ctrl->keep.cube[0], 16, cudaMemcpyDeviceToHost);
+      break;
+    }
+    case BH_EXPORT_KEYS:
+      if (!need(8 * (size_t)c->last_n)) return fail(c, BH_EINVAL, "buffer too small");
+      e = cudaMemcpy(dst, c->sort.keys[c->last_fb], 8 * (size_t)c->last_n, cudaMemcpyDeviceToHost);
+      break;
+    case BH_EXPORT_PERM:
+      if (!need(4 * (size_t)c->last_n)) return fail(c, BH_EINVAL, "buffer too small");
+      e = cudaMemcpy(dst, c->sort.idx[c->last_fb], 4 * (size_t)c->last_n, cudaMemcpyDeviceToHost);
+      break;
+    case BH_EXPORT_TARGET_PERM:
+      if (c->last_self) return fail(c, BH_EINVAL, "last call had no separate targets");
+      if (!need(4 * (size_t)c->last_m)) return fail(c, BH_EINVAL, "buffer too small");
+      e = cudaMemcpy(dst, c->sort_t.idx[c->last_fbt], 4 * (size_t)c->last_m, cudaMemcpyDeviceToHost);
+      break;
+    case BH_EXPORT_NODE_COUNT:
+      if (!need(8)) return fail(c, BH_EINVAL, "buffer too small");
+      memcpy(dst, &nodes, 8);
+      break;
+    case BH_EXPORT_NODES: {
+      if (!need(24 * (size_t)nodes)) return fail(c, BH_EINVAL, "buffer too small");
+      std::vector<int4> topo((size_t)nodes);
+      std::vector<int> par((size_t)nodes);
+      std::vector<unsigned char> lv((size_t)nodes);
+      e = cudaMemcpy(topo.data(), c->build.topo, sizeof(int4) * (size_t)nodes, cudaMemcpyDeviceToHost);
+      if (e == cudaSuccess) e = cudaMemcpy(par.data(), c->build.parent, sizeof(int) * (size_t)nodes, cudaMemcpyDeviceToHost);
+      if (e == cudaSuccess) e = cudaMemcpy(lv.data(), c->build.level, (size_t)nodes, cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) break;
+      int *o = (int *)dst;
+      for (long long k = 0; k < nodes; ++k) {
+        const int4 t = topo[(size_t)k];
+        o[6 * k + 0] = lv[(size_t)k];
+        o[6 * k + 1] = t.x;
+        o[6 * k + 2] = t.y - t.x;
+        o[6 * k + 3] = t.z;
+        o[6 * k + 4] = t.z >= 0 ? t.w - t.z : 0;
+        o[6 * k + 5] = par[(size_t)k];
+      }
+      break;
+    }
+    case BH_EXPORT_COM: {
+      if (!need(16 * (size_t)nodes)) return fail(c, BH_EINVAL, "buffer too small");
+      std::vector<NodeRec> rec((size_t)nodes);
+      e = cudaMemcpy(rec.data(), c->build.rec, sizeof(NodeRec) * (size_t)nodes, cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) break;
+      float *o = (float *)dst;
+      for (long long k = 0; k < nodes; ++k) {
+        o[4 * k + 0] = rec[(size_t)k].com.x;
+        o[4 * k + 1] = rec[(size_t)k].com.y;
+        o[4 * k + 2] = rec[(size_t)k].com.z;
+        o[4 * k + 3] = rec[(size_t)k].com.w;
+      }
+      break;
+    }
+    default:
+      return fail(c, BH_EINVAL, "unknown export key");
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "export copy");
+  return BH_OK;
+}
+
+int bh_count_interactions(bh_ctx *c, unsigned int *counts,
+                          unsigned long long *total, void *stream) {
+  if (!c) return BH_EINVAL;
+  if (!c->last_valid) return fail(c, BH_EINVAL, "no completed bh_compute to count");
+  DeviceGuard g(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_count(c->last_walk, counts, c->ctrl, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "count launch");
+  if (total) {
+    e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(total, &c->ctrl->step.useful, sizeof(unsigned long long),
+                     cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "count read");
+  }
+  return BH_OK;
+}
+
+const char *bh_last_error(const bh_ctx *c) {
+  return c ? c->err.c_str() : "null context";
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Internal declarations shared by the CUDA translation units of libbh.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bh.h"
+
+namespace bh {
+
+// Octree levels 0..21 (21 bits per axis of a 63-bit Morton key).
+constexpr int kMaxBits = 21;
+constexpr int kMaxLevels = kMaxBits + 1;
+constexpr int kMaxPasses = 8;           // 8-bit radix digits of a 63-bit key
+
+// Radix sort tile: 256 threads x 12 keys.
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 12;
+constexpr int kSortTile = kSortThreads * kSortItems;
+
+// Tree build tile: 256 threads x 4 positions.
+constexpr int kBuildThreads = 256;
+constexpr int kBuildIters = 4;
+constexpr int kBuildTile = kBuildThreads * kBuildIters;
+constexpr int kMaxLeafCap = 64;
+
+// Device status word values mirror the public codes.
+constexpr unsigned kErrNonFinite = BH_EINVAL;
+constexpr unsigned kErrTimeout = BH_ETIMEOUT;
+constexpr unsigned kErrOverflow = BH_ETREE_OVERFLOW;
+
+// Per-call control block, zeroed by one cudaMemsetAsync at the start of
+// every bh_compute (so no kernel relies on state left by an earlier call).
+struct StepCtrl {
+  unsigned int hist[2][kMaxPasses][256];   // digit histograms: sources, targets
+  unsigned int tile_ctr[2][kMaxPasses];    // radix tile tickets per pass
+  unsigned int bbox_done[2];               // blocks finished in the bbox pass
+  unsigned int work_ctr;                   // traversal group tickets
+  unsigned int pad0;
+  unsigned long long executed;             // source terms evaluated
+  unsigned long long groups;               // groups walked
+  unsigned long long useful;               // per-target interaction count
+  int level_total[kMaxLevels];             // nodes per level (build scan)
+  int pad1[2];
+};
+
+// Control block kept across calls.
+struct PersistCtrl {
+  unsigned int err;          // first device error code of the call
+  unsigned int epoch;        // bumped once per call; tags look-back slots
+  unsigned int pad[2];
+  float4 cube[2];            // (lo_x, lo_y, lo_z, L): sources, targets
+  float scale[2];            // 2^bits / L, fp32 IEEE division
+  float pad2[2];
+};
+
+struct DevCtrl {
+  StepCtrl step;
+  PersistCtrl keep;
+};
+
+// One traversal record per node, 32 bytes: (com.xyz, mass) and
+// (ropen2 = w^2/theta^2, link, count, flags).  link = first child for an
+// internal node, first particle (sorted index) for a leaf; count = children
+// or particles.  flags bit 0 = leaf; bits 8..15 = level.
+struct alignas(16) NodeRec {
+  float4 com;
+  float ropen2;
+  int link;
+  int count;
+  int flags;
+};
+
+struct SortBufs {
+  unsigned long long *keys[2];
+  unsigned int *idx[2];
+  unsigned long long *status;   // look-back slots, (tiles x 256)
+  int cap_tiles;
+};
+
+// --- launchers (each enqueues on `s`, returns cudaGetLastError()) ---------
+cudaError_t launch_bbox(const float4 *pm, long long n, float4 *partials,
+                        int max_blocks, DevCtrl *ctrl, int which, int bits,
+                        bool bump_epoch, cudaStream_t s);
+cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
+                        DevCtrl *ctrl, int which, int bits, cudaStream_t s);
+// Sorts keys[0] (with implicit iota values); the result lands in
+// keys[final]/idx[final], final returned through *final_buf.
+cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
+                        int which, unsigned spin_limit, int *final_buf,
+                        cudaStream_t s);
+cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
+                          long long n, float4 *out, cudaStream_t s);
+
+struct BuildBufs {
+  int4 *topo;            // (first, end, first_child | -1, child_end)
+  int *parent;
+  unsigned char *level;
+  int *arrive;
+  float4 *msum;          // (sum m x, sum m y, sum m z, sum m)
+  NodeRec *rec;
+  unsigned int *tile_counts;   // [level][tile]
+  long long cap_nodes;
+  int cap_tiles;
+};
+
+cudaError_t launch_build(const unsigned long long *skeys, long long n, int bits,
+                         int leaf_cap, BuildBufs &b, DevCtrl *ctrl,
+                         cudaStream_t s);
+cudaError_t launch_com(const float4 *spm, const unsigned long long *skeys,
+                       long long n, int bits, float theta, BuildBufs &b,
+                       DevCtrl *ctrl, cudaStream_t s);
+
+struct WalkArgs {
+  const float4 *spm;          // sorted sources
+  long long n;                // number of sources
+  const NodeRec *rec;
+  const float4 *tpos;         // targets in walk order
+  const unsigned int *tperm;  // walk order -> caller index
+  long long m;                // number of targets
+  float4 *out;                // caller order
+  float eps2, G;
+  int self_mode;              // targets are the sorted sources
+  int opening;                // BH_OPEN_*
+  int group;                  // 32 or 64
+  int num_sms;
+};
+cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s);
+cudaError_t launch_count(const WalkArgs &a, unsigned int *counts, DevCtrl *ctrl,
+                         cudaStream_t s);
+
+cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
+                          long long m, bool self_mode, float eps, float G,
+                          double *partial, long long partial_cap, float4 *out,
+                          int num_sms, cudaStream_t s);
+
+}  // namespace bh

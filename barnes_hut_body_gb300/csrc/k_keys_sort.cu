@@ -1,0 +1,476 @@
+// Bounding cube, Morton keys and the on-device radix sort.
+//
+// Stages 1-3 of the pipeline of the GASPHiA tree-code page (section
+// "计算核函数": computeBoundingBox) and of the tree page after Burtscher &
+// Pingali (section "实现步骤": bounding box by reduction, then Morton /
+// Z-order keys and a spatial sort so that the 32 threads of a warp hold
+// spatially close particles -- the page's "排序算法" section shows the walk
+// is 10-15x slower without it).
+//
+// GB300 design:
+//  * bbox: one pass of 16-byte loads, grid sized to the SM count; the last
+//    block to finish (ticket counter, no waiting) reduces the block partials
+//    and writes the cube and the quantisation scale.
+//  * keys: fixed fp32 op sequence (round-to-nearest sub, mul; clamp;
+//    truncate) so the integer codes are reproducible bit for bit; the same
+//    pass builds the digit histograms of every radix pass.
+//  * sort: least-significant-digit radix sort, 8-bit digits, one kernel per
+//    digit ("one sweep"): each tile ranks its keys with warp ballots, learns
+//    its global offset by decoupled look-back over the tiles before it (a
+//    bounded wait that flags BH_ETIMEOUT instead of hanging), then scatters
+//    through shared memory so that global writes come out in runs.  Stable,
+//    so equal keys keep the original index order.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bh_internal.h"
+
+namespace bh {
+
+namespace {
+
+__device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
+  atomicCAS(&c->keep.err, 0u, code);
+}
+
+__device__ __forceinline__ bool finite4(float4 p) {
+  return isfinite(p.x) && isfinite(p.y) && isfinite(p.z) && isfinite(p.w);
+}
+
+// ---------------------------------------------------------------------------
+// Bounding cube
+// ---------------------------------------------------------------------------
+constexpr int kBboxThreads = 256;
+
+__global__ void __launch_bounds__(kBboxThreads)
+bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
+            DevCtrl *ctrl, int which, int bits, int bump_epoch) {
+  float lo0 = INFINITY, lo1 = INFINITY, lo2 = INFINITY;
+  float hi0 = -INFINITY, hi1 = -INFINITY, hi2 = -INFINITY;
+  bool bad = false;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    float4 p[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) p[u] = __ldg(pm + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      bad |= !finite4(p[u]);
+      lo0 = fminf(lo0, p[u].x); hi0 = fmaxf(hi0, p[u].x);
+      lo1 = fminf(lo1, p[u].y); hi1 = fmaxf(hi1, p[u].y);
+      lo2 = fminf(lo2, p[u].z); hi2 = fmaxf(hi2, p[u].z);
+    }
+  }
+  for (; i < n; i += stride) {
+    float4 p = __ldg(pm + i);
+    bad |= !finite4(p);
+    lo0 = fminf(lo0, p.x); hi0 = fmaxf(hi0, p.x);
+    lo1 = fminf(lo1, p.y); hi1 = fmaxf(hi1, p.y);
+    lo2 = fminf(lo2, p.z); hi2 = fmaxf(hi2, p.z);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo0 = fminf(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+    lo1 = fminf(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+    lo2 = fminf(lo2, __shfl_xor_sync(0xffffffffu, lo2, o));
+    hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+    hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+    hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  __shared__ float s[6][kBboxThreads / 32];
+  __shared__ int s_bad[kBboxThreads / 32];
+  __shared__ bool s_last;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s[0][w] = lo0; s[1][w] = lo1; s[2][w] = lo2;
+    s[3][w] = hi0; s[4][w] = hi1; s[5][w] = hi2;
+    s_bad[w] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float4 a = make_float4(s[0][0], s[1][0], s[2][0], 0.f);
+    float4 b = make_float4(s[3][0], s[4][0], s[5][0], 0.f);
+    int anybad = s_bad[0];
+    for (int k = 1; k < kBboxThreads / 32; ++k) {
+      a.x = fminf(a.x, s[0][k]); a.y = fminf(a.y, s[1][k]); a.z = fminf(a.z, s[2][k]);
+      b.x = fmaxf(b.x, s[3][k]); b.y = fmaxf(b.y, s[4][k]); b.z = fmaxf(b.z, s[5][k]);
+      anybad |= s_bad[k];
+    }
+    a.w = anybad ? 1.f : 0.f;
+    partials[2 * blockIdx.x] = a;
+    partials[2 * blockIdx.x + 1] = b;
+    __threadfence();
+    unsigned t = atomicAdd(&ctrl->step.bbox_done[which], 1u);
+    s_last = (t == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // Last block: reduce the partials of every block.
+  __threadfence();
+  lo0 = lo1 = lo2 = INFINITY;
+  hi0 = hi1 = hi2 = -INFINITY;
+  bad = false;
+  for (int k = threadIdx.x; k < (int)gridDim.x; k += blockDim.x) {
+    float4 a = __ldcg(partials + 2 * k), b = __ldcg(partials + 2 * k + 1);
+    lo0 = fminf(lo0, a.x); lo1 = fminf(lo1, a.y); lo2 = fminf(lo2, a.z);
+    hi0 = fmaxf(hi0, b.x); hi1 = fmaxf(hi1, b.y); hi2 = fmaxf(hi2, b.z);
+    bad |= (a.w != 0.f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo0 = fminf(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+    lo1 = fminf(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+    lo2 = fminf(lo2, __shfl_xor_sync(0xffffffffu, lo2, o));
+    hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+    hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+    hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  __syncthreads();
+  if (lane == 0) {
+    s[0][w] = lo0; s[1][w] = lo1; s[2][w] = lo2;
+    s[3][w] = hi0; s[4][w] = hi1; s[5][w] = hi2;
+    s_bad[w] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float l[3] = {s[0][0], s[1][0], s[2][0]}, h[3] = {s[3][0], s[4][0], s[5][0]};
+    int anybad = s_bad[0];
+    for (int k = 1; k < kBboxThreads / 32; ++k) {
+      for (int a = 0; a < 3; ++a) {
+        l[a] = fminf(l[a], s[a][k]);
+        h[a] = fmaxf(h[a], s[3 + a][k]);
+      }
+      anybad |= s_bad[k];
+    }
+    // Cube side: the largest extent (fp32 subtraction); 1 if all coincide.
+    float L = 0.f;
+    for (int a = 0; a < 3; ++a) L = fmaxf(L, __fsub_rn(h[a], l[a]));
+    if (L == 0.f) L = 1.f;
+    ctrl->keep.cube[which] = make_float4(l[0], l[1], l[2], L);
+    ctrl->keep.scale[which] = __fdiv_rn((float)(1u << bits), L);
+    if (anybad) set_err(ctrl, kErrNonFinite);
+    if (bump_epoch) ctrl->keep.epoch += 1u;
+    ctrl->step.bbox_done[which] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Morton keys + digit histograms
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long spread3(unsigned int v) {
+  // Insert two zero bits after each of the low 21 bits (Z-order interleave).
+  unsigned long long x = v & 0x1fffffu;
+  x = (x | x << 32) & 0x1f00000000ffffull;
+  x = (x | x << 16) & 0x1f0000ff0000ffull;
+  x = (x | x << 8) & 0x100f00f00f00f00full;
+  x = (x | x << 4) & 0x10c30c30c30c30c3ull;
+  x = (x | x << 2) & 0x1249249249249249ull;
+  return x;
+}
+
+__device__ __forceinline__ unsigned int quantise(float x, float lo, float s,
+                                                 float top) {
+  // (x - lo) * s in round-to-nearest fp32, clamped to [0, 2^bits - 1]
+  // (fmaxf maps NaN, e.g. 0 * inf, to 0), then truncated.
+  float v = __fmul_rn(__fsub_rn(x, lo), s);
+  return __float2uint_rz(fminf(fmaxf(v, 0.f), top));
+}
+
+constexpr int kKeysThreads = 256;
+
+__global__ void __launch_bounds__(kKeysThreads)
+keys_kernel(const float4 *__restrict__ pm, long long n,
+            unsigned long long *__restrict__ keys, DevCtrl *ctrl, int which,
+            int bits) {
+  __shared__ unsigned int h[kMaxPasses][256];
+  for (int k = threadIdx.x; k < kMaxPasses * 256; k += blockDim.x)
+    (&h[0][0])[k] = 0u;
+  __syncthreads();
+  const float4 cube = ctrl->keep.cube[which];
+  const float s = ctrl->keep.scale[which];
+  const float top = (float)((1u << bits) - 1u);
+  const int passes = (3 * bits + 7) / 8;
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = (long long)blockIdx.x * blockDim.x; base < n;
+       base += stride) {
+    long long i = base + threadIdx.x;
+    bool valid = i < n;
+    unsigned long long key = 0;
+    if (valid) {
+      float4 p = __ldg(pm + i);
+      unsigned qx = quantise(p.x, cube.x, s, top);
+      unsigned qy = quantise(p.y, cube.y, s, top);
+      unsigned qz = quantise(p.z, cube.z, s, top);
+      key = spread3(qx) | (spread3(qy) << 1) | (spread3(qz) << 2);
+      keys[i] = key;
+    }
+    for (int ps = 0; ps < passes; ++ps) {
+      unsigned d = (unsigned)(key >> (8 * ps)) & 255u;
+      unsigned tag = valid ? d : 256u + lane;
+      unsigned peers = __match_any_sync(0xffffffffu, tag);
+      if (valid && (peers & ((1u << lane) - 1u)) == 0u)
+        atomicAdd(&h[ps][d], (unsigned)__popc(peers));
+    }
+  }
+  __syncthreads();
+  unsigned int *gh = &ctrl->step.hist[which][0][0];
+  for (int k = threadIdx.x; k < passes * 256; k += blockDim.x) {
+    unsigned v = (&h[0][0])[k];
+    if (v) atomicAdd(gh + k, v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One radix pass (8-bit digit at `shift`)
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kFlagAgg = 1ull << 30;
+constexpr unsigned long long kFlagPrefix = 2ull << 30;
+constexpr unsigned long long kValMask = (1ull << 30) - 1ull;
+
+__device__ __forceinline__ unsigned long long ld_volatile(
+    const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_volatile(unsigned long long *p,
+                                            unsigned long long v) {
+  asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Exclusive block scan of one value per thread (256 threads).
+__device__ __forceinline__ unsigned block_excl_scan256(unsigned v,
+                                                       unsigned *s_warp,
+                                                       unsigned *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  unsigned off = 0, tot = 0;
+#pragma unroll
+  for (int k = 0; k < kSortThreads / 32; ++k) {
+    unsigned c = s_warp[k];
+    if (k < w) off += c;
+    tot += c;
+  }
+  __syncthreads();
+  if (total) *total = tot;
+  return off + x - v;
+}
+
+struct SortSmem {
+  unsigned long long k[kSortTile];
+  unsigned int v[kSortTile];
+};
+
+template <bool kFirst>
+__global__ void __launch_bounds__(kSortThreads)
+sort_pass_kernel(const unsigned long long *__restrict__ kin,
+                 const unsigned int *__restrict__ vin,
+                 unsigned long long *__restrict__ kout,
+                 unsigned int *__restrict__ vout, long long n, int shift,
+                 const unsigned int *__restrict__ hist,
+                 unsigned int *tile_ctr, unsigned long long *status,
+                 unsigned int tag_base, DevCtrl *ctrl,
+                 unsigned int spin_limit) {
+  __shared__ SortSmem st;
+  __shared__ unsigned int s_whist[kSortThreads / 32][256];
+  __shared__ unsigned int s_dig_excl[256];
+  __shared__ unsigned int s_glob[256];
+  __shared__ unsigned int s_warp[kSortThreads / 32];
+  __shared__ unsigned int s_tile;
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const unsigned long long tag =
+      (unsigned long long)(tag_base + ctrl->keep.epoch * 16u) << 32;
+  if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
+  for (int k = tid; k < (kSortThreads / 32) * 256; k += kSortThreads)
+    (&s_whist[0][0])[k] = 0u;
+  // global start of each digit = exclusive scan of this pass's histogram
+  unsigned gofs = block_excl_scan256(hist[tid], s_warp, nullptr);
+  __syncthreads();
+  const long long tile = s_tile;
+  const long long base = tile * kSortTile;
+  const long long wbase = base + (long long)w * (kSortItems * 32);
+
+  unsigned long long key[kSortItems];
+  unsigned int val[kSortItems];
+  unsigned int rnk[kSortItems];
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    long long idx = wbase + i * 32 + lane;
+    bool valid = idx < n;
+    key[i] = valid ? kin[idx] : ~0ull;
+    if (kFirst) val[i] = (unsigned)idx;
+    else val[i] = valid ? vin[idx] : 0u;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    unsigned d = (unsigned)(key[i] >> shift) & 255u;
+    unsigned peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      unsigned bit = (d >> b) & 1u;
+      unsigned bal = __ballot_sync(0xffffffffu, bit);
+      peers &= bit ? bal : ~bal;
+    }
+    unsigned before = s_whist[w][d];
+    rnk[i] = before + __popc(peers & lt);
+    __syncwarp();
+    if ((peers & lt) == 0u) s_whist[w][d] = before + __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per digit: offsets of the warps within the tile, and the tile's count
+  const unsigned d = tid;
+  unsigned run = 0;
+#pragma unroll
+  for (int k = 0; k < kSortThreads / 32; ++k) {
+    unsigned c = s_whist[k][d];
+    s_whist[k][d] = run;
+    run += c;
+  }
+  const unsigned total = run;
+  // decoupled look-back over the tiles before this one
+  unsigned long long *slot = status + tile * 256 + d;
+  unsigned excl = 0;
+  if (tile == 0) {
+    st_volatile(slot, tag | kFlagPrefix | (unsigned long long)total);
+  } else {
+    st_volatile(slot, tag | kFlagAgg | (unsigned long long)total);
+    long long t = tile - 1;
+    unsigned spins = 0;
+    while (t >= 0) {
+      unsigned long long sv = ld_volatile(status + t * 256 + d);
+      if ((sv & 0xffffffff00000000ull) != tag) {
+        if (++spins > spin_limit) {
+          set_err(ctrl, kErrTimeout);
+          break;
+        }
+        if (spins > 64) __nanosleep(32);
+        continue;
+      }
+      excl += (unsigned)(sv & kValMask);
+      if (sv & kFlagPrefix) break;
+      --t;
+    }
+    st_volatile(slot, tag | kFlagPrefix |
+                          ((unsigned long long)(excl + total) & kValMask));
+  }
+  s_glob[d] = gofs + excl;
+  s_dig_excl[d] = block_excl_scan256(total, s_warp, nullptr);
+  __syncthreads();
+  // scatter into shared memory in digit order
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    unsigned dd = (unsigned)(key[i] >> shift) & 255u;
+    unsigned pos = s_dig_excl[dd] + s_whist[w][dd] + rnk[i];
+    st.k[pos] = key[i];
+    st.v[pos] = val[i];
+  }
+  __syncthreads();
+  // write out: consecutive slots of one digit go to consecutive addresses
+  const long long nvalid = n - base < kSortTile ? n - base : kSortTile;
+  for (int j = tid; j < nvalid; j += kSortThreads) {
+    unsigned long long k = st.k[j];
+    unsigned dd = (unsigned)(k >> shift) & 255u;
+    unsigned long long g = (unsigned long long)s_glob[dd] + (j - s_dig_excl[dd]);
+    if (g < (unsigned long long)n) {
+      kout[g] = k;
+      vout[g] = st.v[j];
+    }
+  }
+}
+
+__global__ void gather_kernel(const float4 *__restrict__ in,
+                              const unsigned int *__restrict__ perm,
+                              long long n, float4 *__restrict__ out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n;
+       r += stride) {
+    unsigned p = perm[r];
+    out[r] = (p < (unsigned long long)n) ? __ldg(in + p) : make_float4(0, 0, 0, 0);
+  }
+}
+
+int sm_count() {
+  static int c = 0;
+  if (c == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    if (c <= 0) c = 1;
+  }
+  return c;
+}
+
+}  // namespace
+
+cudaError_t launch_bbox(const float4 *pm, long long n, float4 *partials,
+                        int max_blocks, DevCtrl *ctrl, int which, int bits,
+                        bool bump_epoch, cudaStream_t s) {
+  long long want = (n + kBboxThreads * 4 - 1) / (kBboxThreads * 4);
+  int blocks = (int)(want < max_blocks ? want : max_blocks);
+  if (blocks < 1) blocks = 1;
+  bbox_kernel<<<blocks, kBboxThreads, 0, s>>>(pm, n, partials, ctrl, which,
+                                               bits, bump_epoch ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
+                        DevCtrl *ctrl, int which, int bits, cudaStream_t s) {
+  long long want = (n + kKeysThreads - 1) / kKeysThreads;
+  long long cap = (long long)sm_count() * 8;
+  int blocks = (int)(want < cap ? want : cap);
+  if (blocks < 1) blocks = 1;
+  keys_kernel<<<blocks, kKeysThreads, 0, s>>>(pm, n, keys, ctrl, which, bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
+                        int which, unsigned spin_limit, int *final_buf,
+                        cudaStream_t s) {
+  const int passes = (3 * bits + 7) / 8;
+  const long long tiles = (n + kSortTile - 1) / kSortTile;
+  if (tiles > b.cap_tiles) return cudaErrorInvalidValue;
+  int cur = 0;
+  for (int p = 0; p < passes; ++p) {
+    const unsigned *hist = &ctrl->step.hist[which][p][0];
+    unsigned *ctr = &ctrl->step.tile_ctr[which][p];
+    unsigned tag = (unsigned)(which * 8 + p);
+    if (p == 0)
+      sort_pass_kernel<true><<<(unsigned)tiles, kSortThreads, 0, s>>>(
+          b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, 8 * p,
+          hist, ctr, b.status, tag, ctrl, spin_limit);
+    else
+      sort_pass_kernel<false><<<(unsigned)tiles, kSortThreads, 0, s>>>(
+          b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, 8 * p,
+          hist, ctr, b.status, tag, ctrl, spin_limit);
+    cur ^= 1;
+  }
+  *final_buf = cur;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
+                          long long n, float4 *out, cudaStream_t s) {
+  long long want = (n + 255) / 256;
+  long long cap = (long long)sm_count() * 16;
+  int blocks = (int)(want < cap ? want : cap);
+  if (blocks < 1) blocks = 1;
+  gather_kernel<<<blocks, 256, 0, s>>>(in, perm, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace bh

@@ -1,0 +1,348 @@
+#!/usr/bin/env python
+"""Benchmark of the full Barnes-Hut step on one GB300 (per rank).
+
+A step is one bh_compute: bounding cube -> Morton keys -> radix sort +
+reorder -> octree build -> centre of mass -> warp-cooperative walk -> results
+in caller order, over the whole workload already resident in HBM.  The
+default workload is the 1,000,000-particle lattice (100^3, spacing 0.01,
+masses 1e-6, eps 5e-3, theta 0.5) in shuffled order (permutation seed 1).
+
+metric: useful interactions per second over the full step, where "useful" is
+the per-target Barnes-Hut interaction count (accepted cells + particle
+pairs) of the same tree and theta, counted on the GPU outside the timed
+region.  The group walk evaluates a superset of those terms; the roofline
+object reports the executed terms as fp32 FLOP/s (20 flops per term).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own
+replica of the workload (the path has no exchange step); value is the sum of
+useful interactions over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FLOPS_PER_TERM = 20
+# fp32 peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop
+# (FMA) x 2070 MHz (maximum SM clock).
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+# Our kernels per self-mode step with 63-bit keys: bbox, keys, 8 radix passes,
+# gather, build count/scan/write, centre of mass, walk.
+KERNELS_PER_STEP = {21: 16, 10: 12}
+# DRAM bytes per walk launch from the committed ncu capture of the same
+# kernel (profiles/); None until a capture of the current kernel exists.
+WALK_TRAFFIC_BYTES = None
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="lattice1m_shuffled")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-sample", type=int, default=4096,
+                    help="targets the CPU oracle walks per baseline step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (host logic; exercised by a gloo test on CPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the one leg allowed to run oracle/)
+# ---------------------------------------------------------------------------
+def cpu_oracle_step(src, tgt, G, eps, theta, sample: int, leaf_cap: int = 16):
+    """One oracle step on a bounded sample: the whole build over all sources,
+    then the per-target walk of `sample` targets; the walk time is scaled to
+    all targets.  Returns (seconds for a full step, useful terms per step)."""
+    import numpy as np
+    import oracle as O
+    import workloads as W
+    t0 = time.perf_counter()
+    o = O.OracleBH(src, theta=theta, G=G, eps=eps, leaf_cap=leaf_cap)
+    t1 = time.perf_counter()
+    m = src.shape[0] if tgt is None else tgt.shape[0]
+    idx = W.error_sample(m, sample, seed=5)
+    _, terms = o.bh(tgt, idx=idx)
+    t2 = time.perf_counter()
+    scale = m / idx.shape[0]
+    return (t1 - t0) + (t2 - t1) * scale, float(terms.mean()) * m
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, on this workload."""
+    if rank != 0:
+        return 0
+    import oracle as O
+    import workloads as W
+    src, tgt, G, eps, theta = W.make(args.workload)
+    for _ in range(args.warmup):
+        cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
+    secs, useful = [], 0.0
+    for _ in range(args.steps):
+        s, useful = cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
+        secs.append(s)
+    ms = 1e3 * statistics.mean(secs)
+    value = useful / (ms / 1e3)
+    m = src.shape[0] if tgt is None else tgt.shape[0]
+    sample = (f"build over all {src.shape[0]} sources + per-target walk of "
+              f"{min(args.cpu_sample, m)} sampled targets, walk time scaled to {m}")
+    line = {
+        "impl": "reference", "metric": "useful_interactions_per_s", "value": value,
+        "unit": "interactions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.workload, src, tgt, theta, eps),
+        "cpu_baseline": {"value": value, "unit": "interactions/s", "cores": O.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "interactions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(name, src, tgt, theta, eps):
+    return {"workload": name, "n_sources": int(src.shape[0]),
+            "n_targets": int(src.shape[0] if tgt is None else tgt.shape[0]),
+            "theta": theta, "eps": eps, "opening": "warp vote, groups of 64",
+            "leaf_cap": 16, "key_bits": 63,
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+
+    import barnes_hut_body_gb300 as B
+    import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    src, tgt, G, eps, theta = W.make(args.workload)
+    m = src.shape[0] if tgt is None else tgt.shape[0]
+    d_src = torch.from_numpy(src).to(device)
+    d_tgt = None if tgt is None else torch.from_numpy(tgt).to(device)
+    d_out = torch.empty((m, 4), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1)
+    for _ in range(max(args.warmup, 3)):
+        bh.compute(d_src, d_tgt, d_out)
+    rc = bh.status()
+    if rc != 0:
+        raise RuntimeError(f"warm-up failed: {B.bh_last_error(bh.ctx)}")
+    useful = B.bh_count_interactions(bh.ctx)
+    torch.cuda.synchronize(device)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    stage_ms = []
+    executed = []
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.start()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(float(k))                    # evict L2 (untimed)
+        ev[k][0].record(stream)
+        bh.compute(d_src, d_tgt, d_out)
+        ev[k][1].record(stream)
+        stage_ms.append(B.bh_get_stage_times(bh.ctx))   # waits for the step
+        executed.append(B.bh_get_counters(bh.ctx)[0])
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - wall0
+    barrier(world, device)
+    clocks = sampler.stop() if sampler else None
+    rc = bh.status()
+    if rc != 0:
+        raise RuntimeError(f"timed steps failed: {B.bh_last_error(bh.ctx)}")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(statistics.mean(step_ms), world, device)
+    total_useful = sum_over_ranks(useful, world, device)
+    value = total_useful / (ms / 1e3)
+
+    # end to end through the host-buffer entry point (pinned memory)
+    h_src = torch.from_numpy(src).pin_memory()
+    h_tgt = None if tgt is None else torch.from_numpy(tgt).pin_memory()
+    h_out = torch.empty((m, 4), dtype=torch.float32).pin_memory()
+    B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
+    barrier(world, device)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / args.e2e_steps, world, device)
+    h2d = 16 * (src.shape[0] + (0 if tgt is None else tgt.shape[0]))
+    d2h = 16 * m
+
+    stages = {k: statistics.median([s[k] for s in stage_ms]) for k in stage_ms[0]}
+    walk_ms = stages["traverse"]
+    exec_terms = statistics.median(executed)
+    props = torch.cuda.get_device_properties(device)
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    achieved = exec_terms * FLOPS_PER_TERM / (walk_ms / 1e3) / 1e12
+    launches = KERNELS_PER_STEP[21] * args.steps
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            import oracle as O
+            s, u = cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
+            cpu = {"value": u / s, "unit": "interactions/s", "cores": O.num_threads(),
+                   "kind": "oracle",
+                   "sample": f"build over all {src.shape[0]} sources + per-target walk of "
+                             f"{min(args.cpu_sample, m)} sampled targets, walk time scaled to {m}"}
+        line = {
+            "metric": "useful_interactions_per_s", "value": value, "unit": "interactions/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(args.workload, src, tgt, theta, eps),
+            "stage_ms": {k: round(v, 4) for k, v in stages.items()},
+            "useful_per_step": useful, "executed_per_step": exec_terms,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": WALK_TRAFFIC_BYTES,
+                         "kernel": "walk_kernel<2,vote>",
+                         "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz"},
+            "e2e": {"value": total_useful / (e2e_ms / 1e3), "unit": "interactions/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "wall_s_timed": wall,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    bh.close()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,213 @@
+/*
+ * bh.h -- C ABI of the GB300 Barnes-Hut gravity library (libbh.so).
+ *
+ * One call rebuilds an octree over N fp32 particles and returns, for every
+ * particle (or for every point of a separate target set), the softened
+ * acceleration and potential
+ *
+ *     a_i   = -G sum_j m_j (x_i - x_j) / (|x_i - x_j|^2 + eps^2)^{3/2}
+ *     phi_i = -G sum_j m_j / (|x_i - x_j|^2 + eps^2)^{1/2}
+ *
+ * with a cell replaced by its centre of mass whenever w^2/theta^2 < r^2
+ * (w = the cell's full edge, r = distance from the target to the cell's
+ * centre of mass).  The pipeline and the opening test follow the GASPHiA
+ * tree-code page ("GASPHiA中的自引力树代码效率与优化分析", sections
+ * "计算核函数" and "性能瓶颈分析"); the build steps (bounding box, Morton
+ * keys + spatial sort, octree) follow the tree page after Burtscher &
+ * Pingali ("树结构（基于根据 Burtscher 和 Pingali 的研究）", section
+ * "实现步骤").
+ *
+ * Conventions for every entry point:
+ *  - All functions return an int status (BH_OK = 0, else a BH_E* code).
+ *    bh_last_error() gives a one-line message for the last failure.
+ *  - Particle arrays are AoS fp32 rows (x, y, z, m), 16 bytes per row, the
+ *    base 16-byte aligned.  Result arrays are rows (ax, ay, az, phi).
+ *  - "device" pointers are CUDA device (or managed) memory on the context's
+ *    device; the caller owns them; the library never frees or retains them
+ *    beyond the call's stream work.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device entry points only enqueue work: they return before the
+ *    GPU finishes and perform no host synchronisation, except when a buffer
+ *    must grow (documented at bh_compute).  Errors raised by kernels (a wait
+ *    that timed out, a non-finite input) land in a device status word that
+ *    bh_sync_status() reads.
+ *  - A context is not thread-safe; use one context per host thread/stream.
+ */
+#ifndef BH_H
+#define BH_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bh_ctx bh_ctx;
+
+/* ---- status codes ---- */
+#define BH_OK              0
+#define BH_EINVAL          1   /* bad argument, or non-finite particle data  */
+#define BH_ENOMEM          2   /* device or host allocation failed           */
+#define BH_ECUDA           3   /* a CUDA runtime call or launch failed       */
+#define BH_ETIMEOUT        4   /* a bounded device-side wait gave up         */
+#define BH_ETREE_OVERFLOW  5   /* a node pool or traversal stack was too small */
+
+/* ---- options for bh_set_option ---- */
+#define BH_OPT_KEY_BITS      1  /* bits per axis of the Morton key: 21 (63-bit
+                                   keys, default) or 10 (30-bit keys)        */
+#define BH_OPT_LEAF_CAP      2  /* leaf capacity B in 1..64 (default 16): a
+                                   cell is subdivided while it holds > B     */
+#define BH_OPT_OPENING       3  /* group opening rule, see BH_OPEN_*         */
+#define BH_OPT_TIMING        4  /* 1: record per-stage CUDA events (default 0) */
+#define BH_OPT_GROUP         5  /* targets per warp group: 32 or 64 (default 64) */
+
+#define BH_OPEN_VOTE  0  /* a cell is accepted for a group of targets only if
+                            the opening test holds for every target of the
+                            group (the page's __all_sync warp vote)          */
+#define BH_OPEN_BOX   1  /* accepted if the test holds at the distance from
+                            the centre of mass to the group's bounding box
+                            (implies the vote; cheaper to evaluate)          */
+
+/* ---- debug knobs for bh_set_debug (tests only) ---- */
+#define BH_DBG_SPIN_LIMIT  1    /* polls before a device wait gives up
+                                   (default 1<<22); 0 makes every wait that
+                                   is not already satisfied fail at once    */
+
+/* ---- what bh_debug_export copies (after the stream's work is done) ---- */
+#define BH_EXPORT_CUBE        1  /* float[4]: lo_x, lo_y, lo_z, L            */
+#define BH_EXPORT_KEYS        2  /* uint64[n]: Morton keys in sorted order    */
+#define BH_EXPORT_PERM        3  /* uint32[n]: perm[r] = caller index of the
+                                    r-th particle in key order               */
+#define BH_EXPORT_NODE_COUNT  4  /* int64[1]: number of tree nodes           */
+#define BH_EXPORT_NODES       5  /* int32[6*nodes]: per node (level, first,
+                                    count, first_child or -1, nchild, parent) */
+#define BH_EXPORT_COM         6  /* float[4*nodes]: com x,y,z and mass       */
+#define BH_EXPORT_TARGET_PERM 7  /* uint32[m]: Morton order of the targets   */
+
+/* Stage indices for bh_get_stage_times. */
+#define BH_STAGE_BBOX      0
+#define BH_STAGE_KEYS      1
+#define BH_STAGE_SORT      2
+#define BH_STAGE_REORDER   3
+#define BH_STAGE_BUILD     4
+#define BH_STAGE_COM       5
+#define BH_STAGE_TARGETS   6   /* bbox + keys + sort of a separate target set */
+#define BH_STAGE_TRAVERSE  7   /* walk + write-back in caller order          */
+#define BH_NUM_STAGES      8
+
+/*
+ * Create a context on CUDA device `device` with scratch for up to
+ * `max_sources` particles and `max_targets` separate targets (either may be
+ * 0; buffers grow on demand).  Defaults: theta 0.5, G 1, eps 0, options as
+ * listed above.  *out is set to NULL on failure.
+ */
+int bh_create(bh_ctx **out, int device, size_t max_sources, size_t max_targets);
+
+/* Destroy a context and free its scratch.  NULL is accepted. */
+int bh_destroy(bh_ctx *c);
+
+/*
+ * Physical parameters: opening angle theta >= 0 (theta = 0 never accepts a
+ * cell, reproducing the direct sum), gravitational constant G (finite), and
+ * Plummer softening eps >= 0.  The GASPHiA page passes theta*theta and constG
+ * to its gravity kernel (section "计算核函数"); the softening form is this
+ * library's.  BH_EINVAL if out of range.
+ */
+int bh_set_params(bh_ctx *c, float theta, float G, float eps);
+
+/* Set an option (BH_OPT_*).  BH_EINVAL for an unknown key or bad value. */
+int bh_set_option(bh_ctx *c, int key, long long value);
+
+/* Set a debug knob (BH_DBG_*); for tests of the failure paths. */
+int bh_set_debug(bh_ctx *c, int key, long long value);
+
+/*
+ * Barnes-Hut gravity, the whole pipeline on `stream`: bounding cube ->
+ * Morton keys -> radix sort + reorder -> octree build -> centre of mass ->
+ * warp-cooperative walk -> results written back in caller order.
+ *
+ *   pos_mass  device, n rows (x,y,z,m) -- the sources.
+ *   targets   device, m rows (x,y,z,*) or NULL.  NULL = self-gravity: the
+ *             targets are the sources, each particle's own pair is skipped,
+ *             and m is ignored.
+ *   acc_pot   device, n (self) or m rows (ax,ay,az,phi), written in the same
+ *             order as the particles/targets were given.
+ *
+ * n == 0 writes zeros for any targets and returns BH_OK.  If n (or m)
+ * exceeds the context's capacity the scratch is reallocated first, which
+ * synchronises the device once; all other calls are fully asynchronous and
+ * can be captured in a CUDA graph.  Non-finite positions or masses set
+ * BH_EINVAL in the device status word (results are then unspecified).
+ */
+int bh_compute(bh_ctx *c, const float *pos_mass, size_t n,
+               const float *targets, size_t m, float *acc_pot, void *stream);
+
+/*
+ * Same as bh_compute with HOST buffers: copies the inputs to device staging
+ * buffers owned by the context, computes, copies the results back and
+ * synchronises `stream`.  Pinned (page-locked) host memory makes the copies
+ * asynchronous DMA; pageable memory also works.  Returns the device status.
+ */
+int bh_compute_host(bh_ctx *c, const float *pos_mass, size_t n,
+                    const float *targets, size_t m, float *acc_pot,
+                    void *stream);
+
+/*
+ * Brute-force double loop (the GASPHiA page's 暴力双循环 reference, section
+ * "精度与加速比验证"): every source acts on every target, sums kept in fp32
+ * per tile of sources and in fp64 across tiles.  Same arguments and
+ * conventions as bh_compute.
+ */
+int bh_direct(bh_ctx *c, const float *pos_mass, size_t n,
+              const float *targets, size_t m, float *acc_pot, void *stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word
+ * (BH_OK, BH_EINVAL for non-finite input, BH_ETIMEOUT, BH_ETREE_OVERFLOW).
+ */
+int bh_sync_status(bh_ctx *c, void *stream);
+
+/*
+ * Per-stage milliseconds of the last bh_compute made with BH_OPT_TIMING on
+ * (indices BH_STAGE_*; a stage that did not run reads 0).  Synchronises on
+ * the last recorded event.  n = number of floats at ms (<= BH_NUM_STAGES).
+ */
+int bh_get_stage_times(bh_ctx *c, float *ms, int n);
+
+/*
+ * Interaction counts of the last bh_compute (synchronises the device):
+ * `executed` = source terms evaluated for valid targets by the group walk;
+ * `groups` = number of target groups walked.
+ */
+int bh_get_counters(bh_ctx *c, unsigned long long *executed,
+                    unsigned long long *groups);
+
+/*
+ * Per-target interaction count of the last bh_compute, on `stream`: for every
+ * target, the number of terms (accepted cells + particle pairs, own pair
+ * excluded) that a walk deciding the opening test per target -- the
+ * textbook Barnes-Hut rule of the GASPHiA page's section "性能瓶颈分析"
+ * without the warp vote -- evaluates on the same tree.  This is the minimum
+ * work at this theta; the group walk of bh_compute evaluates a superset.
+ * counts: device uint32[targets] in caller order, or NULL.  total: host, or
+ * NULL; if given, `stream` is synchronised and the sum written.  The last
+ * call's sources and targets must still be resident and unchanged.
+ */
+int bh_count_interactions(bh_ctx *c, unsigned int *counts,
+                          unsigned long long *total, void *stream);
+
+/*
+ * Copy internal state of the last bh_compute to host memory (synchronises
+ * the device).  `what` is a BH_EXPORT_* key; `bytes` is the size of
+ * host_dst, which must hold the whole item (BH_EINVAL otherwise).
+ */
+int bh_debug_export(bh_ctx *c, int what, void *host_dst, size_t bytes);
+
+/* Message for the last failed call on this context ("" if none). */
+const char *bh_last_error(const bh_ctx *c);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BH_H */
