@@ -26,7 +26,7 @@ BH_OPT_KEY_BITS, BH_OPT_LEAF_CAP, BH_OPT_OPENING, BH_OPT_TIMING, BH_OPT_GROUP = 
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
 BH_DBG_SPIN_LIMIT = 1
 (BH_EXPORT_CUBE, BH_EXPORT_KEYS, BH_EXPORT_PERM, BH_EXPORT_NODE_COUNT,
- BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM) = range(1, 8)
+ BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM, BH_EXPORT_WALK_STATS) = range(1, 9)
 STAGES = ("bbox", "keys", "sort", "reorder", "build", "com", "targets", "traverse")
 
 EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
@@ -213,6 +213,8 @@ def bh_debug_export(ctx, what: int, count: int = 0) -> np.ndarray:
         out = np.zeros((count, 6), np.int32)
     elif what == BH_EXPORT_COM:
         out = np.zeros((count, 4), np.float32)
+    elif what == BH_EXPORT_WALK_STATS:
+        out = np.zeros(4, np.uint64)
     else:
         raise ValueError("unknown export key")
     _check(ctx, lib().bh_debug_export(ctx, int(what), C.c_void_p(out.ctypes.data), out.nbytes))

@@ -532,6 +532,10 @@ int bh_debug_export(bh_ctx *c, int what, void *dst, size_t bytes) {
       if (!need(4 * (size_t)c->last_m)) return fail(c, BH_EINVAL, "buffer too small");
       e = cudaMemcpy(dst, c->sort_t.idx[c->last_fbt], 4 * (size_t)c->last_m, cudaMemcpyDeviceToHost);
       break;
+    case BH_EXPORT_WALK_STATS:
+      if (!need(32)) return fail(c, BH_EINVAL, "buffer too small");
+      memcpy(dst, st.walk_stats, 32);
+      break;
     case BH_EXPORT_NODE_COUNT:
       if (!need(8)) return fail(c, BH_EINVAL, "buffer too small");
       memcpy(dst, &nodes, 8);

@@ -40,6 +40,8 @@ struct StepCtrl {
   unsigned long long executed;             // source terms evaluated
   unsigned long long groups;               // groups walked
   unsigned long long useful;               // per-target interaction count
+  unsigned long long walk_stats[4];        // rounds, nodes tested, nodes put
+                                           // to the vote, leaf chunks
   int level_total[kMaxLevels];             // nodes per level (build scan)
   int pad1[2];
 };

@@ -23,9 +23,11 @@
 //  * Accepted nodes (centre of mass + mass) and the particles of opened
 //    leaves are appended to a per-warp interaction list in shared memory;
 //    opened internal nodes push their child range.  Whenever 64 entries are
-//    waiting, the warp evaluates them for all its targets: each entry is one
-//    broadcast shared-memory read followed by 3 sub, 3 FMA, 1 rsqrt, 3 mul,
-//    3 FMA and 1 add per target -- no divergence, no per-lane branching.
+//    waiting, the warp evaluates them for all its targets with Blackwell's
+//    packed fp32x2 instructions: two entries per 64-bit operand, so a pair of
+//    entries costs two broadcast shared-memory reads and, per target, 13
+//    packed ops (3 sub, 3 fma, 3 mul, 3 fma, 1 sub) plus 2 rsqrt -- no
+//    divergence, no per-lane branching.
 //  * Self mode: a target's own particle, when it comes through an opened
 //    leaf, adds exactly m*rsqrt(eps^2) to its potential and nothing to its
 //    acceleration; the walk records which targets saw their own particle and
@@ -46,11 +48,16 @@ constexpr int kWalkWarps = 8;
 constexpr int kWalkThreads = kWalkWarps * 32;
 constexpr int kStackCap = 736;   // >= 28 * 22 + 32: pops >= 1 range of <= 8
                                  // per round, pushes <= 32, depth <= 22
-constexpr int kListCap = 96;
+constexpr int kListCap = 96;    // entries; stored as pairs (see below)
 constexpr int kFlushAt = 64;
 
+// The interaction list holds entries (x, y, z, m) two by two, each pair as
+// two 16-byte words: (x_j, x_j+1, y_j, y_j+1) and (z_j, z_j+1, m_j, m_j+1).
+// One broadcast 16-byte shared load then yields two packed fp32x2 operands.
 struct WarpSmem {
-  float4 list[kListCap];
+  ulonglong2 list[kListCap / 2][2];
+  float4 cand[32];                    // candidates put to the vote
+  float4 probe[8];                    // probe targets of the group
   unsigned int stack[kStackCap];
 };
 
@@ -58,51 +65,102 @@ __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
   atomicCAS(&c->keep.err, 0u, code);
 }
 
+// ---- packed fp32x2 arithmetic (two fp32 lanes per 64-bit register) -------
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(f2 v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Append entry j (x, y, z, m) to the paired list.
+__device__ __forceinline__ void list_put(WarpSmem &S, int j, float4 v) {
+  float *w = reinterpret_cast<float *>(&S.list[j >> 1][0]);
+  const int h = j & 1;
+  w[h] = v.x;
+  w[2 + h] = v.y;
+  w[4 + h] = v.z;
+  w[6 + h] = v.w;
+}
+
+// Targets are held duplicated in both fp32 lanes (P = (p, p)); a pair of
+// entries then gives two interactions per packed instruction.  Per pair and
+// target: 3 sub, 3 fma, 2 rsqrt, 3 mul, 3 fma, 1 sub (13 packed + 2 MUFU).
 template <int T, bool kEps0>
-__device__ __forceinline__ void interact(const float4 e, const float (&px)[T],
-                                         const float (&py)[T],
-                                         const float (&pz)[T], float eps2,
-                                         float (&ax)[T], float (&ay)[T],
-                                         float (&az)[T], float (&ph)[T]) {
+struct Acc {
+  f2 px[T], py[T], pz[T];     // targets, duplicated in both lanes
+  f2 ax[T], ay[T], az[T], ph[T];
+  f2 eps2;
+
+  __device__ __forceinline__ void pair(const ulonglong2 a, const ulonglong2 b) {
+    // a = (xx, yy), b = (zz, mm)
 #pragma unroll
-  for (int k = 0; k < T; ++k) {
-    float dx = e.x - px[k];
-    float dy = e.y - py[k];
-    float dz = e.z - pz[k];
-    float r2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, eps2)));
-    float inv = rsqrtf(r2);
-    if (kEps0) inv = (r2 > 0.f) ? inv : 0.f;
-    float minv = e.w * inv;
-    float minv3 = minv * (inv * inv);
-    ax[k] = fmaf(dx, minv3, ax[k]);
-    ay[k] = fmaf(dy, minv3, ay[k]);
-    az[k] = fmaf(dz, minv3, az[k]);
-    ph[k] -= minv;
+    for (int k = 0; k < T; ++k) {
+      f2 dx = sub2(a.x, px[k]);
+      f2 dy = sub2(a.y, py[k]);
+      f2 dz = sub2(b.x, pz[k]);
+      f2 r2 = fma2(dx, dx, fma2(dy, dy, fma2(dz, dz, eps2)));
+      float r0, r1;
+      upk(r2, r0, r1);
+      float i0 = rsqrtf(r0), i1 = rsqrtf(r1);
+      if (kEps0) {
+        i0 = (r0 > 0.f) ? i0 : 0.f;
+        i1 = (r1 > 0.f) ? i1 : 0.f;
+      }
+      f2 inv = pk(i0, i1);
+      f2 minv = mul2(b.y, inv);
+      f2 minv3 = mul2(minv, mul2(inv, inv));
+      ax[k] = fma2(dx, minv3, ax[k]);
+      ay[k] = fma2(dy, minv3, ay[k]);
+      az[k] = fma2(dz, minv3, az[k]);
+      ph[k] = sub2(ph[k], minv);
+    }
   }
-}
 
-template <int T, bool kEps0>
-__device__ __forceinline__ void flush_full(const float4 *list,
-                                           const float (&px)[T],
-                                           const float (&py)[T],
-                                           const float (&pz)[T], float eps2,
-                                           float (&ax)[T], float (&ay)[T],
-                                           float (&az)[T], float (&ph)[T]) {
-#pragma unroll 8
-  for (int j = 0; j < kFlushAt; ++j)
-    interact<T, kEps0>(list[j], px, py, pz, eps2, ax, ay, az, ph);
-}
+  // Evaluate list pairs [0, npairs).
+  __device__ __forceinline__ void run(const WarpSmem &S, int npairs) {
+#pragma unroll 2
+    for (int p = 0; p < npairs; ++p) pair(S.list[p][0], S.list[p][1]);
+  }
+  __device__ __forceinline__ void run_full(const WarpSmem &S) {
+#pragma unroll 2
+    for (int p = 0; p < kFlushAt / 2; ++p) pair(S.list[p][0], S.list[p][1]);
+  }
+};
 
+// Evaluate the first kFlushAt list entries and move the rest to the front.
 template <int T, bool kEps0>
-__device__ __forceinline__ void flush_part(const float4 *list, int cnt,
-                                           const float (&px)[T],
-                                           const float (&py)[T],
-                                           const float (&pz)[T], float eps2,
-                                           float (&ax)[T], float (&ay)[T],
-                                           float (&az)[T], float (&ph)[T]) {
-#pragma unroll 4
-  for (int j = 0; j < cnt; ++j)
-    interact<T, kEps0>(list[j], px, py, pz, eps2, ax, ay, az, ph);
+__device__ __forceinline__ void flush_front(WarpSmem &S, Acc<T, kEps0> &accum,
+                                            int &nl, int nvalid,
+                                            unsigned long long &executed) {
+  const int lane = threadIdx.x & 31;
+  accum.run_full(S);
+  executed += (unsigned long long)kFlushAt * nvalid;
+  nl -= kFlushAt;
+  __syncwarp();
+  if (lane < (nl + 1) / 2) {
+    S.list[lane][0] = S.list[kFlushAt / 2 + lane][0];
+    S.list[lane][1] = S.list[kFlushAt / 2 + lane][1];
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
@@ -124,6 +182,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
   constexpr int GS = 32 * T;
   const long long ngroups = (a.m + GS - 1) / GS;
   unsigned long long executed = 0, ngroup_done = 0;
+  unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0;
   long long nnodes = 0;
   for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
 
@@ -135,7 +194,9 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
     const long long t0 = (long long)g * GS;
     const int nvalid = (int)((a.m - t0) < GS ? (a.m - t0) : GS);
 
-    float px[T], py[T], pz[T], ax[T], ay[T], az[T], ph[T];
+    float px[T], py[T], pz[T];
+    Acc<T, kEps0> accum;
+    accum.eps2 = pk(a.eps2, a.eps2);
     bool valid[T], selfhit[T];
     float bl0 = INFINITY, bl1 = INFINITY, bl2 = INFINITY;
     float bh0 = -INFINITY, bh1 = -INFINITY, bh2 = -INFINITY;
@@ -145,7 +206,11 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       valid[k] = t < a.m;
       float4 p = __ldg(a.tpos + (valid[k] ? t : t0));
       px[k] = p.x; py[k] = p.y; pz[k] = p.z;
-      ax[k] = ay[k] = az[k] = ph[k] = 0.f;
+      accum.px[k] = pk(p.x, p.x);
+      accum.py[k] = pk(p.y, p.y);
+      accum.pz[k] = pk(p.z, p.z);
+      if ((lane & 7) == 0) S.probe[k * 4 + (lane >> 3)] = make_float4(p.x, p.y, p.z, 0.f);
+      accum.ax[k] = accum.ay[k] = accum.az[k] = accum.ph[k] = 0ull;
       selfhit[k] = false;
       bl0 = fminf(bl0, p.x); bh0 = fmaxf(bh0, p.x);
       bl1 = fminf(bl1, p.y); bh1 = fmaxf(bh1, p.y);
@@ -190,45 +255,65 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       const int eexcl = __shfl_sync(0xffffffffu, excl, e);
       const unsigned node = ebase + (unsigned)(lane - eexcl);
       __syncwarp();
+      ++st_rounds;
+      st_tested += (unsigned)total;
 
-      // ---- load the candidate's record and test it ---------------------
-      float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      float ro2 = 0.f;
-      int link = 0, count = 0, flags = 0;
-      bool acc = false;
+      // ---- issue the candidates' record loads ----------------------------
       if (has && node >= nnodes) {     // only after a failed earlier stage
         has = false;
         set_err(ctrl, kErrOverflow);
       }
+      float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
       if (has) {
         const float4 *r = reinterpret_cast<const float4 *>(a.rec + node);
         c4 = __ldg(r);
-        float4 q = __ldg(r + 1);
-        ro2 = q.x;
-        link = __float_as_int(q.y);
-        count = __float_as_int(q.z);
-        flags = __float_as_int(q.w);
+        q = __ldg(r + 1);
+      }
+      // ---- evaluate a full list while the loads are in flight -------------
+      if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
+
+      // ---- opening test ---------------------------------------------------
+      const float ro2 = q.x;
+      const int link = __float_as_int(q.y);
+      int count = __float_as_int(q.z);
+      const int flags = __float_as_int(q.w);
+      bool acc = false;
+      if (has) {
         float dx = fmaxf(fmaxf(bl0 - c4.x, c4.x - bh0), 0.f);
         float dy = fmaxf(fmaxf(bl1 - c4.y, c4.y - bh1), 0.f);
         float dz = fmaxf(fmaxf(bl2 - c4.z, c4.z - bh2), 0.f);
         acc = ro2 < fmaf(dx, dx, fmaf(dy, dy, dz * dz));
       }
       if (kVote) {
-        unsigned cand = __ballot_sync(0xffffffffu, has && !acc);
+        // Probe pre-test: if one of the probe targets (real targets of the
+        // group) fails the opening test, the vote fails; same arithmetic as
+        // the vote, so the outcome is identical, only cheaper.
+        bool und = has && !acc;
+        if (__any_sync(0xffffffffu, und)) {
+#pragma unroll
+          for (int k = 0; k < 4 * T; ++k) {
+            const float4 pr = S.probe[k];
+            float dx = c4.x - pr.x, dy = c4.y - pr.y, dz = c4.z - pr.z;
+            float r2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+            und = und && (ro2 < r2);
+          }
+        }
+        unsigned cand = __ballot_sync(0xffffffffu, und);
+        st_voted += __popc(cand);
+        if (und) S.cand[lane] = make_float4(c4.x, c4.y, c4.z, ro2);
+        __syncwarp();
         unsigned accm = 0;
         while (cand) {
           const int c = __ffs(cand) - 1;
           cand &= cand - 1u;
-          const float cx = __shfl_sync(0xffffffffu, c4.x, c);
-          const float cy = __shfl_sync(0xffffffffu, c4.y, c);
-          const float cz = __shfl_sync(0xffffffffu, c4.z, c);
-          const float r2o = __shfl_sync(0xffffffffu, ro2, c);
+          const float4 cd = S.cand[c];
           bool ok = true;
 #pragma unroll
           for (int k = 0; k < T; ++k) {
-            float dx = cx - px[k], dy = cy - py[k], dz = cz - pz[k];
+            float dx = cd.x - px[k], dy = cd.y - py[k], dz = cd.z - pz[k];
             float r2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
-            ok = ok && (!valid[k] || r2o < r2);
+            ok = ok && (!valid[k] || cd.w < r2);
           }
           if (__all_sync(0xffffffffu, ok)) accm |= 1u << c;
         }
@@ -246,7 +331,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
 
       // ---- accepted nodes -> interaction list ---------------------------
       const unsigned am = __ballot_sync(0xffffffffu, has && acc);
-      if (has && acc) S.list[nl + __popc(am & lt)] = c4;
+      if (has && acc) list_put(S, nl + __popc(am & lt), c4);
       nl += __popc(am);
 
       // ---- opened internal nodes -> stack -------------------------------
@@ -261,14 +346,6 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
         if (lane == 0) set_err(ctrl, kErrOverflow);
       }
       __syncwarp();
-      if (nl >= kFlushAt) {
-        flush_full<T, kEps0>(S.list, px, py, pz, a.eps2, ax, ay, az, ph);
-        executed += (unsigned long long)kFlushAt * nvalid;
-        nl -= kFlushAt;
-        __syncwarp();
-        if (lane < nl) S.list[lane] = S.list[kFlushAt + lane];
-        __syncwarp();
-      }
 
       // ---- opened leaves -> their particles -----------------------------
       const unsigned lm = __ballot_sync(0xffffffffu, open_leaf);
@@ -298,32 +375,31 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
             selfhit[k] = selfhit[k] || (((k == 0 ? m0 : m1) >> lane) & 1u);
         }
         for (int base = 0; base < ptotal; base += 32) {
-          const int q = base + lane;
+          ++st_chunks;
+          const int qi = base + lane;
           int lo = 0;
 #pragma unroll
           for (int s = 16; s >= 1; s >>= 1) {
             int v = __shfl_sync(0xffffffffu, ppre, lo + s - 1);
-            if (v <= q) lo += s;
+            if (v <= qi) lo += s;
           }
           const int owner = lo > 31 ? 31 : lo;
           const int of = __shfl_sync(0xffffffffu, link, owner);
           const int oe = __shfl_sync(0xffffffffu, pexcl, owner);
-          if (q < ptotal) S.list[nl + lane] = __ldg(a.spm + of + (q - oe));
+          float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (qi < ptotal) pv = __ldg(a.spm + of + (qi - oe));
+          if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
+          if (qi < ptotal) list_put(S, nl + lane, pv);
           nl += (ptotal - base < 32) ? (ptotal - base) : 32;
           __syncwarp();
-          if (nl >= kFlushAt) {
-            flush_full<T, kEps0>(S.list, px, py, pz, a.eps2, ax, ay, az, ph);
-            executed += (unsigned long long)kFlushAt * nvalid;
-            nl -= kFlushAt;
-            __syncwarp();
-            if (lane < nl) S.list[lane] = S.list[kFlushAt + lane];
-            __syncwarp();
-          }
         }
       }
     }
+    if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
     if (nl > 0) {
-      flush_part<T, kEps0>(S.list, nl, px, py, pz, a.eps2, ax, ay, az, ph);
+      if ((nl & 1) && lane == 0) list_put(S, nl, make_float4(0.f, 0.f, 0.f, 0.f));
+      __syncwarp();
+      accum.run(S, (nl + 1) / 2);
       executed += (unsigned long long)nl * nvalid;
     }
     __syncwarp();
@@ -331,20 +407,31 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
     for (int k = 0; k < T; ++k) {
       if (!valid[k]) continue;
       const long long t = t0 + k * 32 + lane;
+      float x0, x1, y0, y1, z0, z1, p0, p1;
+      upk(accum.ax[k], x0, x1);
+      upk(accum.ay[k], y0, y1);
+      upk(accum.az[k], z0, z1);
+      upk(accum.ph[k], p0, p1);
+      float ph = p0 + p1;
       if (kSelf && !kEps0 && selfhit[k]) {
         // undo the self pair: it added m * rsqrt(eps^2) to -phi
         const float m_self = __ldg(a.tpos + t).w;
-        ph[k] += m_self * rsqrtf(a.eps2);
+        ph += m_self * rsqrtf(a.eps2);
       }
       const unsigned ci = a.tperm ? a.tperm[t] : (unsigned)t;
       if (ci < (unsigned long long)a.m)
-        a.out[ci] = make_float4(a.G * ax[k], a.G * ay[k], a.G * az[k], a.G * ph[k]);
+        a.out[ci] = make_float4(a.G * (x0 + x1), a.G * (y0 + y1), a.G * (z0 + z1),
+                                a.G * ph);
     }
     ++ngroup_done;
   }
   if (lane == 0) {
     atomicAdd(&ctrl->step.executed, executed);
     atomicAdd(&ctrl->step.groups, ngroup_done);
+    atomicAdd(&ctrl->step.walk_stats[0], st_rounds);
+    atomicAdd(&ctrl->step.walk_stats[1], st_tested);
+    atomicAdd(&ctrl->step.walk_stats[2], st_voted);
+    atomicAdd(&ctrl->step.walk_stats[3], st_chunks);
   }
 }
 

@@ -83,6 +83,8 @@ typedef struct bh_ctx bh_ctx;
                                     count, first_child or -1, nchild, parent) */
 #define BH_EXPORT_COM         6  /* float[4*nodes]: com x,y,z and mass       */
 #define BH_EXPORT_TARGET_PERM 7  /* uint32[m]: Morton order of the targets   */
+#define BH_EXPORT_WALK_STATS  8  /* uint64[4]: walk rounds, nodes tested,
+                                    nodes decided by the vote, leaf chunks   */
 
 /* Stage indices for bh_get_stage_times. */
 #define BH_STAGE_BBOX      0
