@@ -68,7 +68,7 @@ def lib():
         L.orc_bh_group.argtypes = [_f32p, C.c_int64, _i32p, _i64p, _i64p, _i64p,
                                    _i32p, _f64p, C.c_double, C.c_double, C.c_double,
                                    C.c_double, _f32p, _vp, C.c_int64, C.c_int64,
-                                   C.c_int, _f64p, _vp]
+                                   C.c_int, _f64p, _vp, _vp]
         L.orc_num_threads.restype = C.c_int
         L.orc_set_threads.argtypes = [C.c_int]
         _LIB = L
@@ -239,14 +239,16 @@ class OracleBH:
         t = _rows(tgt)
         return sort(keys(t, bbox(t), self.bits)).astype(np.int64)
 
-    def bh_group(self, tgt=None, group=32, mode=0, groups=None, theta=None):
+    def bh_group(self, tgt=None, group=32, mode=0, groups=None, theta=None,
+                 with_abs=False):
         """Group walk over Morton-ordered targets.
 
         mode 0: a cell is accepted iff every target of the group accepts it
         (the warp vote); mode 1: iff the test holds at the distance from the
         centre of mass to the group's bounding box.  ``groups``: indices of the
         groups to evaluate (default all).  Returns (out rows, original target
-        indices of those rows, terms per evaluated group).
+        indices of those rows, terms per evaluated group), plus, with
+        ``with_abs``, G * sum |acceleration term| per row.
         """
         args = list(self._walk_args())
         if theta is not None:
@@ -266,8 +268,11 @@ class OracleBH:
         k = pos.shape[0]
         out = np.zeros((k, 4), np.float64)
         terms = np.zeros(gsel.size, np.int64)
+        absacc = np.zeros(k, np.float64)
         lib().orc_bh_group(*args, pos, _ptr(selfj), k, int(group), int(mode), out,
-                           terms.ctypes.data_as(C.c_void_p))
+                           terms.ctypes.data_as(C.c_void_p), absacc.ctypes.data_as(C.c_void_p))
+        if with_abs:
+            return out, rows, terms, absacc
         return out, rows, terms
 
     def direct(self, tgt=None, idx=None):

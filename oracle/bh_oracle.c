@@ -266,6 +266,16 @@ static inline void pair_term(const double *x, double sx, double sy, double sz,
     acc[3] -= m * inv;
 }
 
+/* Magnitude of the acceleration term of one pair (for error scales). */
+static inline double pair_mag(const double *x, double sx, double sy, double sz,
+                              double m, double eps2)
+{
+    double dx = sx - x[0], dy = sy - x[1], dz = sz - x[2];
+    double r2 = dx * dx + dy * dy + dz * dz + eps2;
+    if (r2 == 0.0) return 0.0;
+    return fabs(m) * sqrt(dx * dx + dy * dy + dz * dz) / (r2 * sqrt(r2));
+}
+
 /* ------------------------------------------------------------------------ */
 /* Brute-force double loop ([T] 精度与加速比验证: 暴力计算 reference).           */
 /* tgt == NULL: self mode over the sources (pair j == i skipped).            */
@@ -371,7 +381,9 @@ void orc_bh(const float *spm, int64_t nnodes, const int32_t *level,
 /* __all_sync), or if it holds for the distance from the centre of mass to   */
 /* the group's bounding box (mode 1: box test, which implies mode 0).        */
 /* Every accepted cell and every particle of an opened leaf is applied to    */
-/* every target of the group.  Targets are given in group order.             */
+/* every target of the group.  Targets are given in group order.  absacc     */
+/* (may be NULL) receives, per target, G * sum |acceleration term|: the scale */
+/* of the rounding error of any summation of the same terms.                 */
 /* ------------------------------------------------------------------------ */
 void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                   const int64_t *first, const int64_t *count,
@@ -379,14 +391,14 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                   const double *com, double L, double theta, double G,
                   double eps, const float *tgt_pos, const int64_t *self_j,
                   int64_t k, int64_t group, int mode, double *out,
-                  int64_t *terms)
+                  int64_t *terms, double *absacc)
 {
     double th2 = theta * theta, eps2 = eps * eps;
     int64_t ngroups = (k + group - 1) / group;
 #pragma omp parallel
     {
         int64_t *stack = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nnodes + 8));
-        double *acc = (double *)malloc(sizeof(double) * 4 * (size_t)group);
+        double *acc = (double *)malloc(sizeof(double) * 5 * (size_t)group);
 #pragma omp for schedule(dynamic, 4)
         for (int64_t g = 0; g < ngroups; ++g) {
             int64_t t0 = g * group, t1 = t0 + group < k ? t0 + group : k;
@@ -398,7 +410,8 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                     if (v < blo[a]) blo[a] = v;
                     if (v > bhi[a]) bhi[a] = v;
                 }
-            memset(acc, 0, sizeof(double) * 4 * (size_t)group);
+            memset(acc, 0, sizeof(double) * 5 * (size_t)group);
+            double *mag = acc + 4 * (size_t)group;
             int64_t nterm = 0, sp = 0;
             stack[sp++] = 0;
             while (sp > 0) {
@@ -428,6 +441,7 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                     for (int64_t r = t0; r < t1; ++r) {
                         double x[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
                         pair_term(x, cm[0], cm[1], cm[2], cm[3], eps2, acc + 4 * (r - t0));
+                        mag[r - t0] += pair_mag(x, cm[0], cm[1], cm[2], cm[3], eps2);
                     }
                     nterm += t1 - t0;
                 } else if (child[c] < 0) {
@@ -437,6 +451,7 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                             if (self_j && self_j[r] == j) continue;
                             double x[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
                             pair_term(x, p[0], p[1], p[2], p[3], eps2, acc + 4 * (r - t0));
+                            mag[r - t0] += pair_mag(x, p[0], p[1], p[2], p[3], eps2);
                         }
                     }
                     nterm += count[c] * (t1 - t0);
@@ -445,8 +460,10 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
                         stack[sp++] = child[c] + q;
                 }
             }
-            for (int64_t r = t0; r < t1; ++r)
+            for (int64_t r = t0; r < t1; ++r) {
                 for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[4 * (r - t0) + a];
+                if (absacc) absacc[r] = fabs(G) * mag[r - t0];
+            }
             if (terms) terms[g] = nterm;
         }
         free(acc);

@@ -29,8 +29,8 @@ def _check_full(name, src, tgt, G, eps, theta, sample, ngroups_sample=256):
     g, ostats = H.assert_error_no_worse(got[idx], per_target, direct, name)
     ng = (m + 63) // 64
     gsel = np.sort(W.rng(13).choice(ng, size=min(ngroups_sample, ng), replace=False))
-    ref, rows, _ = o.bh_group(tgt, group=64, mode=0, groups=gsel)
-    H.assert_walk_close(got[rows], ref, name)
+    ref, rows, _, mag = o.bh_group(tgt, group=64, mode=0, groups=gsel, with_abs=True)
+    H.assert_walk_close(got[rows], ref, name, mag)
     return g, ostats
 
 

@@ -102,8 +102,8 @@ def test_walk_matches_oracle_group_walk(name, theta, group, opening):
     bh, got, rc = H.gpu_bh(src, theta=theta, G=G, eps=eps, group=group, opening=opening)
     assert rc == 0
     o = O.OracleBH(src, theta=theta, G=G, eps=eps, leaf_cap=16)
-    ref, rows, _ = o.bh_group(group=group, mode=opening)
-    H.assert_walk_close(got[rows], ref, f"{name} th={theta} g={group} m={opening}")
+    ref, rows, _, mag = o.bh_group(group=group, mode=opening, with_abs=True)
+    H.assert_walk_close(got[rows], ref, f"{name} th={theta} g={group} m={opening}", mag)
     idx = W.error_sample(src.shape[0], 2048)
     direct = o.direct(idx=idx)
     per_target, _ = o.bh(idx=idx)
@@ -130,8 +130,8 @@ def test_source_target_walk(opening):
     tperm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, tgt.shape[0])
     o = O.OracleBH(src, theta=0.5, G=1.0, eps=1e-4, leaf_cap=16)
     np.testing.assert_array_equal(tperm, o.target_order(tgt))
-    ref, rows, _ = o.bh_group(tgt, group=64, mode=opening)
-    H.assert_walk_close(got[rows], ref, "surface")
+    ref, rows, _, mag = o.bh_group(tgt, group=64, mode=opening, with_abs=True)
+    H.assert_walk_close(got[rows], ref, "surface", mag)
     direct = o.direct(tgt)
     per_target, _ = o.bh(tgt)
     H.assert_error_no_worse(got, per_target, direct, "surface")
@@ -142,8 +142,8 @@ def test_eps_zero():
     _, got, rc = H.gpu_bh(src, theta=0.5, eps=0.0)
     assert rc == 0
     o = O.OracleBH(src, theta=0.5, eps=0.0, leaf_cap=16)
-    ref, rows, _ = o.bh_group(group=64, mode=0)
-    H.assert_walk_close(got[rows], ref, "eps0")
+    ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
+    H.assert_walk_close(got[rows], ref, "eps0", mag)
     dgot, rc = H.gpu_direct(src, eps=0.0)
     assert rc == 0
     H.assert_direct_close(dgot, O.direct(src, None, 1.0, 0.0))
@@ -155,8 +155,8 @@ def test_walk_other_leaf_caps(leaf_cap):
     _, got, rc = H.gpu_bh(src, theta=0.5, leaf_cap=leaf_cap)
     assert rc == 0
     o = O.OracleBH(src, theta=0.5, leaf_cap=leaf_cap)
-    ref, rows, _ = o.bh_group(group=64, mode=0)
-    H.assert_walk_close(got[rows], ref, f"B={leaf_cap}")
+    ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
+    H.assert_walk_close(got[rows], ref, f"B={leaf_cap}", mag)
 
 
 def test_gravity_constant_and_thirty_bit_keys():
@@ -164,8 +164,8 @@ def test_gravity_constant_and_thirty_bit_keys():
     _, got, rc = H.gpu_bh(src, theta=0.6, G=2.5, eps=2e-3, key_bits=10)
     assert rc == 0
     o = O.OracleBH(src, theta=0.6, G=2.5, eps=2e-3, bits=10, leaf_cap=16)
-    ref, rows, _ = o.bh_group(group=64, mode=0)
-    H.assert_walk_close(got[rows], ref, "G=2.5 bits=10")
+    ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
+    H.assert_walk_close(got[rows], ref, "G=2.5 bits=10", mag)
 
 
 @pytest.mark.parametrize("name", ["uniform4096", "plummer_2e15", "galaxy_2e16"])
