@@ -32,7 +32,8 @@ STAGES = ("bbox", "keys", "sort", "reorder", "build", "com", "targets", "travers
 EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
             "bh_set_debug", "bh_compute", "bh_compute_host", "bh_direct",
             "bh_sync_status", "bh_get_stage_times", "bh_get_counters",
-            "bh_debug_export", "bh_count_interactions", "bh_last_error")
+            "bh_debug_export", "bh_count_interactions", "bh_direct_static",
+            "bh_last_error")
 
 _lib = None
 
@@ -65,6 +66,7 @@ def lib():
         L.bh_get_counters.argtypes = [vp, C.POINTER(C.c_ulonglong), C.POINTER(C.c_ulonglong)]
         L.bh_debug_export.argtypes = [vp, i, vp, sz]
         L.bh_count_interactions.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), vp]
+        L.bh_direct_static.argtypes = [vp, sz, vp, sz, f, f, vp, vp]
         L.bh_last_error.argtypes = [vp]
         L.bh_last_error.restype = C.c_char_p
         for name in EXPORTED:
@@ -149,6 +151,28 @@ def bh_direct(ctx, pos_mass, targets, acc_pot, stream=None) -> None:
     if k != (n if targets is None else m):
         raise ValueError("acc_pot has the wrong number of rows")
     _check(ctx, lib().bh_direct(ctx, p, n, t, m, o, _stream(pos_mass, stream)))
+
+
+def bh_direct_static(pos_mass, targets, acc_pot, G: float = 1.0, eps: float = 0.0,
+                     stream=None) -> None:
+    """Brute-force sum with no device allocation and no context.
+
+    For callers that cannot allocate GPU memory where they need forces (a
+    CUDA graph being captured, a loop that must not synchronise the device,
+    a program that pools all GPU memory itself).  Scratch is an 8 MiB array
+    built into the library: at most 262,144 targets per call, and calls that
+    overlap on the GPU race.  The first call on a device should come before
+    any stream capture.
+    """
+    p, n = _rows_ptr(pos_mass, "pos_mass")
+    t, m = _rows_ptr(targets, "targets")
+    o, k = _rows_ptr(acc_pot, "acc_pot")
+    if k != (n if targets is None else m):
+        raise ValueError("acc_pot has the wrong number of rows")
+    rc = lib().bh_direct_static(p, n, t, m, float(G), float(eps), o, _stream(pos_mass, stream))
+    if rc != BH_OK:
+        raise BHError(rc, "bh_direct_static failed (bad argument, more than "
+                          "262144 targets, or a CUDA error)")
 
 
 def _host_rows(a, name):

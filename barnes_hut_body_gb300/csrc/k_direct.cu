@@ -12,7 +12,10 @@
 // blockIdx.y; every split writes its fp64 partial sums and a second kernel
 // adds the splits in a fixed order (deterministic).
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "bh_internal.h"
 
@@ -138,4 +141,79 @@ cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free entry point
+//
+// bh_direct_static serves callers that cannot allocate device memory when
+// they need forces: code running while a CUDA graph is being captured
+// (cudaMalloc is not allowed there), loops that must never synchronise the
+// device (cudaMalloc and cudaFree can), and host programs that hand all GPU
+// memory to their own pool at start-up.  It needs no context: its only
+// scratch -- the fp64 partial sums of the source splits -- lives in a
+// file-scope device array that every GPU loading the library keeps until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr long long kStaticScratchDoubles = 1LL << 20;   // 8 MiB
+constexpr int kStaticMaxDevices = 64;
+
+static __device__ __align__(256) double g_static_partial[kStaticScratchDoubles];
+
+std::mutex g_static_mu;
+double *g_static_addr[kStaticMaxDevices] = {};
+int g_static_sms[kStaticMaxDevices] = {};
+
+}  // namespace
+
 }  // namespace bh
+
+extern "C" int bh_direct_static(const float *pos_mass, size_t n,
+                                const float *targets, size_t m, float G,
+                                float eps, float *acc_pot, void *stream) {
+  using namespace bh;
+  const bool self = targets == nullptr;
+  const long long N = (long long)n, M = self ? N : (long long)m;
+  auto bad_rows = [](const float *p, long long rows) {
+    return rows > 0 && (p == nullptr || ((uintptr_t)p & 15u) != 0);
+  };
+  if (bad_rows(pos_mass, N) || (!self && bad_rows(targets, M)) || bad_rows(acc_pot, M))
+    return BH_EINVAL;
+  if (!isfinite(G) || !(eps >= 0.f) || !isfinite(eps)) return BH_EINVAL;
+  if (M == 0) return BH_OK;
+  if (4 * M > kStaticScratchDoubles) return BH_EINVAL;   // > 262,144 targets
+  cudaStream_t s = (cudaStream_t)stream;
+  if (N == 0)
+    return cudaMemsetAsync(acc_pot, 0, sizeof(float4) * (size_t)M, s) == cudaSuccess
+               ? BH_OK : BH_ECUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices)
+    return BH_ECUDA;
+  double *scratch = nullptr;
+  int sms = 1;
+  {
+    // Set-up, once per device with that device current: the host name of
+    // g_static_partial is only a stand-in, the kernels need its device
+    // address.  The first call on a device does this, so it should come
+    // before any stream capture.
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_partial) != cudaSuccess || !p)
+        return BH_ECUDA;
+      int c = 0;
+      if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return BH_ECUDA;
+      g_static_sms[dev] = c > 0 ? c : 1;
+      g_static_addr[dev] = static_cast<double *>(p);
+    }
+    scratch = g_static_addr[dev];
+    sms = g_static_sms[dev];
+  }
+  cudaError_t e = launch_direct(reinterpret_cast<const float4 *>(pos_mass), N,
+                                reinterpret_cast<const float4 *>(self ? pos_mass : targets),
+                                M, self, eps, G, scratch, kStaticScratchDoubles,
+                                reinterpret_cast<float4 *>(acc_pot), sms, s);
+  return e == cudaSuccess ? BH_OK : BH_ECUDA;
+}
+

@@ -164,6 +164,31 @@ int bh_direct(bh_ctx *c, const float *pos_mass, size_t n,
               const float *targets, size_t m, float *acc_pot, void *stream);
 
 /*
+ * Allocation-free brute-force sum, for callers that cannot allocate device
+ * memory at the point where they need forces: code running while a CUDA
+ * graph is being captured, loops that must never synchronise the device
+ * (cudaMalloc/cudaFree may), and programs whose GPU memory is handed to
+ * their own pool at start-up.  The pages have no counterpart of this entry
+ * point; it is the bh_direct computation without a context.
+ *
+ *   pos_mass, targets, acc_pot: as in bh_direct (device, 16-byte aligned;
+ *   targets NULL = self mode, own pair skipped).  G finite, eps >= 0.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Its only
+ * scratch is a file-scope device array of 8 MiB (fp64 partial sums), held
+ * by every GPU that loads the library until the process exits; at most
+ * 262,144 targets per call (more returns BH_EINVAL).  The first call on a
+ * device looks up the array's device address (make it before any stream
+ * capture).  Every call shares the one array, so calls that overlap on the
+ * GPU (other streams, other host threads) race and give wrong results;
+ * serialise them.  Returns BH_OK, BH_EINVAL (bad pointer, alignment,
+ * parameter or size) or BH_ECUDA.
+ */
+int bh_direct_static(const float *pos_mass, size_t n, const float *targets,
+                     size_t m, float G, float eps, float *acc_pot,
+                     void *stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word
  * (BH_OK, BH_EINVAL for non-finite input, BH_ETIMEOUT, BH_ETREE_OVERFLOW).
  */
