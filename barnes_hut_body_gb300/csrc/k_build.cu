@@ -136,7 +136,10 @@ build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
     long long j = tb + it * kBuildThreads + threadIdx.x;
     int s, L, e, Lp;
     position_facts(g, n, tb, j, B, bits, s, L, e, Lp);
-    for (int l = 0; l <= bits; ++l) {
+    // only the levels some position of this warp starts a cell at
+    const int lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(s <= L ? s : bits + 1));
+    const int hi = __reduce_max_sync(0xffffffffu, L < 0 ? 0 : L);
+    for (int l = lo; l <= hi; ++l) {
       unsigned b = __ballot_sync(0xffffffffu, s <= l && l <= L);
       if (lane == l) mine += __popc(b);
     }
@@ -211,15 +214,19 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
     s_ok = off <= cap_nodes;
     if (!s_ok && blockIdx.x == 0) set_err(ctrl, kErrOverflow);
   }
+  for (int k = threadIdx.x; k < kBuildIters * kLvWarps * kMaxLevels; k += blockDim.x)
+    (&s_cnt[0][0][0])[k] = 0u;
   load_geom(g, skeys, n, tb, B, bits);
   if (!s_ok) return;
-  // phase A: per (iteration, warp, level) counts
+  // phase A: per (iteration, warp, level) counts, over the warp's levels only
   int s[kBuildIters], L[kBuildIters], e[kBuildIters], Lp[kBuildIters];
 #pragma unroll
   for (int it = 0; it < kBuildIters; ++it) {
     long long j = tb + it * kBuildThreads + threadIdx.x;
     position_facts(g, n, tb, j, B, bits, s[it], L[it], e[it], Lp[it]);
-    for (int l = 0; l <= bits; ++l) {
+    const int lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(s[it] <= L[it] ? s[it] : bits + 1));
+    const int hi = __reduce_max_sync(0xffffffffu, L[it] < 0 ? 0 : L[it]);
+    for (int l = lo; l <= hi; ++l) {
       unsigned b = __ballot_sync(0xffffffffu, s[it] <= l && l <= L[it]);
       if (lane == 0) s_cnt[it][w][l] = __popc(b);
     }
@@ -247,7 +254,13 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
     // offset included); st[l] = whether one starts at j.
     long long r_m1 = 0, r_0 = 0;
     bool st_m1 = false, st_0 = false;
-    for (int l = 0; l <= bits + 1; ++l) {
+    // Levels with a write in this warp: starts in [s, L], ends in (e, Lp].
+    const int wlo = (int)__reduce_min_sync(
+        0xffffffffu, (unsigned)min(sj <= Lj ? sj : bits + 1, ej + 1 <= Lpj ? ej + 1 : bits + 1));
+    const int whi = __reduce_max_sync(0xffffffffu, (unsigned)max(max(Lj, Lpj), 0));
+    const int l_first = wlo > 0 ? wlo - 1 : 0;
+    const int l_last = whi + 1 < bits + 1 ? whi + 1 : bits + 1;
+    for (int l = l_first; l <= l_last; ++l) {
       long long r_p1 = 0;
       bool st_p1 = false;
       if (l <= bits) {
@@ -258,7 +271,7 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
       }
       // handle level lv = l - 1 using ranks of lv - 1 (r_m1), lv (r_0), lv + 1 (r_p1)
       const int lv = l - 1;
-      if (lv >= 0) {
+      if (lv >= wlo && lv >= 0) {
         if (st_0) {                              // a cell of level lv starts at j
           long long idx = r_0;
           if (idx >= 0 && idx < cap_nodes) {
@@ -304,8 +317,8 @@ __device__ void finish_node(long long c, float4 sum, int lvl, int link,
   NodeRec r;
   const float w = ldexpf(cube.w, -lvl);            // full cell edge
   if (sum.w != 0.f) {
-    r.com = make_float4(__fdiv_rn(sum.x, sum.w), __fdiv_rn(sum.y, sum.w),
-                        __fdiv_rn(sum.z, sum.w), sum.w);
+    const float inv = __frcp_rn(sum.w);
+    r.com = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w);
   } else {                                          // massless: cell centre
     unsigned long long key = skeys[first_particle];
     const int sh = bits - lvl;
@@ -344,7 +357,20 @@ com_kernel(const float4 *__restrict__ spm, const unsigned long long *skeys,
     long long e = t.y < f ? f : t.y;
     if (e > n) e = n;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long long j = f; j < e; ++j) {
+    long long j = f;
+    for (; j + 4 <= e; j += 4) {          // four loads in flight
+      float4 p[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) p[u] = __ldg(spm + j + u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        s.x = fmaf(p[u].w, p[u].x, s.x);
+        s.y = fmaf(p[u].w, p[u].y, s.y);
+        s.z = fmaf(p[u].w, p[u].z, s.z);
+        s.w += p[u].w;
+      }
+    }
+    for (; j < e; ++j) {
       float4 p = __ldg(spm + j);
       s.x = fmaf(p.w, p.x, s.x);
       s.y = fmaf(p.w, p.y, s.y);

@@ -209,12 +209,17 @@ keys_kernel(const float4 *__restrict__ pm, long long n,
       key = spread3(qx) | (spread3(qy) << 1) | (spread3(qz) << 2);
       keys[i] = key;
     }
+    // Spatially ordered input makes whole warps share the high digits: add
+    // those with one atomic; otherwise every lane adds its own.
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
     for (int ps = 0; ps < passes; ++ps) {
-      unsigned d = (unsigned)(key >> (8 * ps)) & 255u;
-      unsigned tag = valid ? d : 256u + lane;
-      unsigned peers = __match_any_sync(0xffffffffu, tag);
-      if (valid && (peers & ((1u << lane) - 1u)) == 0u)
-        atomicAdd(&h[ps][d], (unsigned)__popc(peers));
+      const unsigned d = (unsigned)(key >> (8 * ps)) & 255u;
+      const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
+      if (__all_sync(0xffffffffu, !valid || d == d0)) {
+        if (lane == 0) atomicAdd(&h[ps][d0], (unsigned)__popc(vmask));
+      } else if (valid) {
+        atomicAdd(&h[ps][d], 1u);
+      }
     }
   }
   __syncthreads();
@@ -231,6 +236,7 @@ keys_kernel(const float4 *__restrict__ pm, long long n,
 constexpr unsigned long long kFlagAgg = 1ull << 30;
 constexpr unsigned long long kFlagPrefix = 2ull << 30;
 constexpr unsigned long long kValMask = (1ull << 30) - 1ull;
+constexpr int kLookback = 8;     // predecessor slots read per round trip
 
 __device__ __forceinline__ unsigned long long ld_volatile(
     const unsigned long long *p) {
@@ -349,21 +355,35 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
     st_volatile(slot, tag | kFlagPrefix | (unsigned long long)total);
   } else {
     st_volatile(slot, tag | kFlagAgg | (unsigned long long)total);
+    // Read a window of predecessors per round trip: when a wave of tiles
+    // starts together, the nearest inclusive prefix can be far back.
     long long t = tile - 1;
     unsigned spins = 0;
-    while (t >= 0) {
-      unsigned long long sv = ld_volatile(status + t * 256 + d);
-      if ((sv & 0xffffffff00000000ull) != tag) {
+    bool done = false;
+    while (t >= 0 && !done) {
+      unsigned long long w[kLookback];
+#pragma unroll
+      for (int k = 0; k < kLookback; ++k)
+        w[k] = (t - k >= 0) ? ld_volatile(status + (t - k) * 256 + d)
+                            : (tag | kFlagPrefix);
+      int used = 0;
+#pragma unroll
+      for (int k = 0; k < kLookback; ++k) {
+        if (done || used < k) break;
+        const unsigned long long sv = w[k];
+        if ((sv & 0xffffffff00000000ull) != tag) break;   // not published yet
+        if (t - k >= 0) excl += (unsigned)(sv & kValMask);
+        used = k + 1;
+        if ((sv & kFlagPrefix) || t - k <= 0) done = true;
+      }
+      t -= used;
+      if (!done && used == 0) {
         if (++spins > spin_limit) {
           set_err(ctrl, kErrTimeout);
           break;
         }
         if (spins > 64) __nanosleep(32);
-        continue;
       }
-      excl += (unsigned)(sv & kValMask);
-      if (sv & kFlagPrefix) break;
-      --t;
     }
     st_volatile(slot, tag | kFlagPrefix |
                           ((unsigned long long)(excl + total) & kValMask));
@@ -431,7 +451,7 @@ cudaError_t launch_bbox(const float4 *pm, long long n, float4 *partials,
 cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
                         DevCtrl *ctrl, int which, int bits, cudaStream_t s) {
   long long want = (n + kKeysThreads - 1) / kKeysThreads;
-  long long cap = (long long)sm_count() * 8;
+  long long cap = (long long)sm_count() * 4;
   int blocks = (int)(want < cap ? want : cap);
   if (blocks < 1) blocks = 1;
   keys_kernel<<<blocks, kKeysThreads, 0, s>>>(pm, n, keys, ctrl, which, bits);
