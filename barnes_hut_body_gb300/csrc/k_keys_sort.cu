@@ -461,6 +461,18 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
                         int which, unsigned spin_limit, int *final_buf,
                         cudaStream_t s) {
+  static bool carveout = false;
+  if (!carveout) {
+    // ~47 KB of shared memory per tile: ask for the largest shared carveout
+    // so that more than two tiles fit on an SM.
+    cudaFuncSetAttribute(sort_pass_kernel<true>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(sort_pass_kernel<false>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    carveout = true;
+  }
   const int passes = (3 * bits + 7) / 8;
   const long long tiles = (n + kSortTile - 1) / kSortTile;
   if (tiles > b.cap_tiles) return cudaErrorInvalidValue;

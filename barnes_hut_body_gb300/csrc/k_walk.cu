@@ -50,6 +50,7 @@ constexpr int kStackCap = 736;   // >= 28 * 22 + 32: pops >= 1 range of <= 8
                                  // per round, pushes <= 32, depth <= 22
 constexpr int kListCap = 96;    // entries; stored as pairs (see below)
 constexpr int kFlushAt = 64;
+constexpr int kProbesPerSlot = 4;   // probe targets per 32-target slot
 
 // The interaction list holds entries (x, y, z, m) two by two, each pair as
 // two 16-byte words: (x_j, x_j+1, y_j, y_j+1) and (z_j, z_j+1, m_j, m_j+1).
@@ -209,7 +210,8 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       accum.px[k] = pk(p.x, p.x);
       accum.py[k] = pk(p.y, p.y);
       accum.pz[k] = pk(p.z, p.z);
-      if ((lane & 7) == 0) S.probe[k * 4 + (lane >> 3)] = make_float4(p.x, p.y, p.z, 0.f);
+      if ((lane & (32 / kProbesPerSlot - 1)) == 0)
+        S.probe[k * kProbesPerSlot + lane / (32 / kProbesPerSlot)] = make_float4(p.x, p.y, p.z, 0.f);
       accum.ax[k] = accum.ay[k] = accum.az[k] = accum.ph[k] = 0ull;
       selfhit[k] = false;
       bl0 = fminf(bl0, p.x); bh0 = fmaxf(bh0, p.x);
@@ -292,7 +294,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
         bool und = has && !acc;
         if (__any_sync(0xffffffffu, und)) {
 #pragma unroll
-          for (int k = 0; k < 4 * T; ++k) {
+          for (int k = 0; k < kProbesPerSlot * T; ++k) {
             const float4 pr = S.probe[k];
             float dx = c4.x - pr.x, dy = c4.y - pr.y, dz = c4.z - pr.z;
             float r2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
@@ -354,10 +356,13 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
         const int ppre = warp_incl_scan(pc, lane);
         const int ptotal = __shfl_sync(0xffffffffu, ppre, 31);
         const int pexcl = ppre - pc;
-        if (kSelf) {
-          // which targets of the group see their own particle
+        // which targets of the group see their own particle (only leaves
+        // holding some of the group's own targets can)
+        const bool mine = kSelf && open_leaf && pc > 0 && (long long)link < t0 + GS &&
+                          (long long)link + pc > t0;
+        if (kSelf && __any_sync(0xffffffffu, mine)) {
           unsigned long long msk = 0ull;
-          if (open_leaf && pc > 0) {
+          if (mine) {
             long long lo = (long long)link - t0, hi = lo + pc;
             if (lo < 0) lo = 0;
             if (hi > GS) hi = GS;

@@ -56,10 +56,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="lattice1m_shuffled")
+    ap.add_argument("--theta", type=float, default=None,
+                    help="override the workload's opening angle")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample", type=int, default=4096,
                     help="targets the CPU oracle walks per baseline step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--direct", action="store_true",
+                    help="time the brute-force kernel (bh_direct) on the workload instead")
     return ap.parse_args()
 
 
@@ -187,6 +191,7 @@ def run_reference(args, rank, world):
     import oracle as O
     import workloads as W
     src, tgt, G, eps, theta = W.make(args.workload)
+    theta = args.theta if args.theta is not None else theta
     for _ in range(args.warmup):
         cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
     secs, useful = [], 0.0
@@ -213,6 +218,32 @@ def run_reference(args, rank, world):
     return 0
 
 
+def measured_hbm_gbs() -> float:
+    """HBM copy bandwidth measured on this GPU pool (generated file),
+    else the fallback figure for a GB300."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return 6800.0
+
+
+def stage_bytes(n: int, m: int, nodes: int, self_mode: bool) -> dict:
+    """Algorithmic DRAM bytes of each build-side stage for one step (63-bit
+    keys, 8 radix passes): what the stage must read and write at least."""
+    b = {
+        "bbox": 16 * n,                          # read particles
+        "keys": 16 * n + 8 * n,                  # read particles, write keys
+        "sort": 8 * 24 * n,                      # per pass: key+index in and out
+        "reorder": 4 * n + 16 * n + 16 * n,      # perm, gather, write
+        "build": 2 * 8 * n + 25 * nodes,         # keys twice; topology written
+        "com": 16 * n + 69 * nodes,              # particles; topology in, records out
+    }
+    if not self_mode:
+        b["targets"] = 16 * m + 24 * m + 8 * 24 * m + 36 * m
+    return b
+
+
 def workload_config(name, src, tgt, theta, eps):
     return {"workload": name, "n_sources": int(src.shape[0]),
             "n_targets": int(src.shape[0] if tgt is None else tgt.shape[0]),
@@ -235,6 +266,7 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.set_device(device)
     dist_init(world, "nccl")
     src, tgt, G, eps, theta = W.make(args.workload)
+    theta = args.theta if args.theta is not None else theta
     m = src.shape[0] if tgt is None else tgt.shape[0]
     d_src = torch.from_numpy(src).to(device)
     d_tgt = None if tgt is None else torch.from_numpy(tgt).to(device)
@@ -295,6 +327,10 @@ def run_ours(args, rank, local_rank, world):
 
     stages = {k: statistics.median([s[k] for s in stage_ms]) for k in stage_ms[0]}
     walk_ms = stages["traverse"]
+    nodes = int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_NODE_COUNT)[0])
+    sbytes = stage_bytes(src.shape[0], m, nodes, tgt is None)
+    hbm_peak = measured_hbm_gbs()
+    stage_gbs = {k: sbytes[k] / (stages[k] * 1e-3) / 1e9 for k in sbytes if stages.get(k, 0) > 0}
     exec_terms = statistics.median(executed)
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
@@ -317,7 +353,10 @@ def run_ours(args, rank, local_rank, world):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(args.workload, src, tgt, theta, eps),
             "stage_ms": {k: round(v, 4) for k, v in stages.items()},
-            "useful_per_step": useful, "executed_per_step": exec_terms,
+            "useful_per_step": useful, "executed_per_step": exec_terms, "nodes": nodes,
+            "stage_hbm": {"unit": "GB/s", "peak": hbm_peak,
+                          "achieved": {k: round(v, 1) for k, v in stage_gbs.items()},
+                          "frac": {k: round(v / hbm_peak, 3) for k, v in stage_gbs.items()}},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": WALK_TRAFFIC_BYTES,
@@ -336,11 +375,65 @@ def run_ours(args, rank, local_rank, world):
     return 0
 
 
+def run_direct(args, rank, local_rank, world):
+    """Brute-force kernel on the workload: pairs/s and its fp32 roofline."""
+    import torch
+
+    import barnes_hut_body_gb300 as B
+    import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    src, tgt, G, eps, theta = W.make(args.workload)
+    theta = args.theta if args.theta is not None else theta
+    n = src.shape[0]
+    m = n if tgt is None else tgt.shape[0]
+    pairs = n * (n - 1) if tgt is None else n * m
+    d_src = torch.from_numpy(src).to(device)
+    d_tgt = None if tgt is None else torch.from_numpy(tgt).to(device)
+    d_out = torch.empty((m, 4), dtype=torch.float32, device=device)
+    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank)
+    for _ in range(max(args.warmup, 3)):
+        bh.direct(d_src, d_tgt, d_out)
+    if bh.status() != 0:
+        raise RuntimeError(B.bh_last_error(bh.ctx))
+    stream = torch.cuda.current_stream(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        bh.direct(d_src, d_tgt, d_out)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
+    props = torch.cuda.get_device_properties(device)
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    achieved = pairs * FLOPS_PER_TERM / (ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "direct_pairs_per_s", "value": sum_over_ranks(pairs, world, device) / (ms / 1e3),
+            "unit": "pairs/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "n_sources": n, "n_targets": m, "eps": eps,
+                       "kernel": "direct (fp32 tiles, fp64 across tiles)"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None},
+            "gpu_launches": 2 * args.steps}), flush=True)
+    bh.close()
+    return 0
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.direct:
+        return run_direct(args, rank, local_rank, world)
     return run_ours(args, rank, local_rank, world)
 
 
