@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbh.so")
 
 BH_OK, BH_EINVAL, BH_ENOMEM, BH_ECUDA, BH_ETIMEOUT, BH_ETREE_OVERFLOW = range(6)
-BH_OPT_KEY_BITS, BH_OPT_LEAF_CAP, BH_OPT_OPENING, BH_OPT_TIMING, BH_OPT_GROUP = 1, 2, 3, 4, 5
+BH_OPT_KEY_BITS, BH_OPT_LEAF_CAP, BH_OPT_OPENING, BH_OPT_TIMING, BH_OPT_GROUP, BH_OPT_GRAPH = 1, 2, 3, 4, 5, 6
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
 BH_DBG_SPIN_LIMIT = 1
 (BH_EXPORT_CUBE, BH_EXPORT_KEYS, BH_EXPORT_PERM, BH_EXPORT_NODE_COUNT,
@@ -279,13 +279,15 @@ class BarnesHut:
         self.device = device
         bh_set_params(self.ctx, theta, G, eps)
         names = dict(key_bits=BH_OPT_KEY_BITS, leaf_cap=BH_OPT_LEAF_CAP,
-                     opening=BH_OPT_OPENING, timing=BH_OPT_TIMING, group=BH_OPT_GROUP)
+                     opening=BH_OPT_OPENING, timing=BH_OPT_TIMING, group=BH_OPT_GROUP,
+                     graph=BH_OPT_GRAPH)
         for k, v in options.items():
             bh_set_option(self.ctx, names[k], v)
 
     def set_option(self, key: str, value: int) -> None:
         names = dict(key_bits=BH_OPT_KEY_BITS, leaf_cap=BH_OPT_LEAF_CAP,
-                     opening=BH_OPT_OPENING, timing=BH_OPT_TIMING, group=BH_OPT_GROUP)
+                     opening=BH_OPT_OPENING, timing=BH_OPT_TIMING, group=BH_OPT_GROUP,
+                     graph=BH_OPT_GRAPH)
         bh_set_option(self.ctx, names[key], value)
 
     def set_params(self, theta, G, eps) -> None:

@@ -53,6 +53,24 @@ struct bh_ctx {
 
   WalkArgs last_walk{};
   long long last_n = 0, last_m = 0;
+
+  // CUDA graph of the whole step, replayed when a call repeats exactly.
+  struct Key {
+    const void *pm, *tg;
+    void *out;
+    long long n, m, cap_n, cap_m;
+    float theta, G, eps;
+    int bits, leaf_cap, opening, group;
+    unsigned spin;
+    bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
+  };
+  int use_graph = 1;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  Key gkey{}, prev_key{};
+  bool has_prev = false;
+  int g_fb = 0, g_fbt = 0;
+  WalkArgs g_walk{};
   int last_fb = 0, last_fbt = 0;
   bool last_self = true, last_valid = false;
 };
@@ -198,6 +216,60 @@ void record(bh_ctx *c, int i, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+
+// Enqueue every stage of one step on `s` (no host synchronisation).
+cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
+                         const float4 *tg, long long M, float4 *out, bool self,
+                         cudaStream_t s, int *fb_out, int *fbt_out,
+                         WalkArgs *walk_out) {
+  cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
+  if (e != cudaSuccess) return e;
+  record(c, 0, s);
+  int fb = 0, fbt = 0;
+  e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
+  record(c, 1, s);
+  if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
+  record(c, 2, s);
+  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
+  record(c, 3, s);
+  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
+  record(c, 4, s);
+  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
+  record(c, 5, s);
+  if (e == cudaSuccess) e = launch_com(c->spm, c->sort.keys[fb], N, c->bits, c->theta, c->build, c->ctrl, s);
+  record(c, 6, s);
+  if (!self) {
+    if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->bits, false, s);
+    if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->bits, s);
+    if (e == cudaSuccess) e = launch_sort(c->sort_t, M, c->bits, c->ctrl, 1, c->spin_limit, &fbt, s);
+    if (e == cudaSuccess) e = launch_gather(tg, c->sort_t.idx[fbt], M, c->stm, s);
+  }
+  record(c, 7, s);
+  WalkArgs a;
+  a.spm = c->spm;
+  a.n = N;
+  a.rec = c->build.rec;
+  a.tpos = self ? c->spm : c->stm;
+  a.tperm = self ? c->sort.idx[fb] : c->sort_t.idx[fbt];
+  a.m = M;
+  a.out = out;
+  a.eps2 = c->eps * c->eps;
+  a.G = c->G;
+  a.self_mode = self ? 1 : 0;
+  a.opening = c->opening;
+  a.group = c->group;
+  a.num_sms = c->num_sms;
+  if (e == cudaSuccess) e = launch_walk(a, c->ctrl, s);
+  record(c, 8, s);
+  *fb_out = fb;
+  *fbt_out = fbt;
+  *walk_out = a;
+  return e;
+}
+
+}  // namespace
+
 extern "C" {
 
 int bh_create(bh_ctx **out, int device, size_t max_sources, size_t max_targets) {
@@ -220,6 +292,7 @@ int bh_create(bh_ctx **out, int device, size_t max_sources, size_t max_targets) 
   if (ok && max_sources) ok = ensure_sources(c, (long long)max_sources) == BH_OK;
   if (ok && max_targets) ok = ensure_targets(c, (long long)max_targets) == BH_OK;
   if (ok) ok = ensure_status(c, 1) == BH_OK;
+  if (ok) ok = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (!ok) {
     bh_destroy(c);
     return BH_ENOMEM;
@@ -244,6 +317,8 @@ int bh_destroy(bh_ctx *c) {
     free_dev(c->stage_out);
     for (int i = 0; i <= BH_NUM_STAGES; ++i)
       if (c->ev[i]) cudaEventDestroy(c->ev[i]);
+    if (c->gexec) cudaGraphExecDestroy(c->gexec);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   }
   delete c;
   return BH_OK;
@@ -277,6 +352,9 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       return BH_OK;
     case BH_OPT_TIMING:
       c->timing = v ? 1 : 0;
+      return BH_OK;
+    case BH_OPT_GRAPH:
+      c->use_graph = v ? 1 : 0;
       return BH_OK;
     case BH_OPT_GROUP:
       if (v != 32 && v != 64) return fail(c, BH_EINVAL, "group must be 32 or 64");
@@ -322,49 +400,59 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   const float4 *tg = reinterpret_cast<const float4 *>(targets);
   float4 *out = reinterpret_cast<float4 *>(acc_pot);
   for (int i = 0; i < BH_NUM_STAGES; ++i) c->stage_ran[i] = false;
-
-  cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
-  if (e != cudaSuccess) return cuda_fail(c, e, "memset");
-  record(c, 0, s);
   int fb = 0, fbt = 0;
-  e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
-  record(c, 1, s);
-  if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
-  record(c, 2, s);
-  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
-  record(c, 3, s);
-  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
-  record(c, 4, s);
-  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
-  record(c, 5, s);
-  if (e == cudaSuccess) e = launch_com(c->spm, c->sort.keys[fb], N, c->bits, c->theta, c->build, c->ctrl, s);
-  record(c, 6, s);
-  if (!self) {
-    if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->bits, false, s);
-    if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->bits, s);
-    if (e == cudaSuccess) e = launch_sort(c->sort_t, M, c->bits, c->ctrl, 1, c->spin_limit, &fbt, s);
-    if (e == cudaSuccess) e = launch_gather(tg, c->sort_t.idx[fbt], M, c->stm, s);
+  WalkArgs walk{};
+  cudaError_t e = cudaSuccess;
+
+  // Repeated identical calls replay one CUDA graph of the whole step: the
+  // second identical call captures it on an internal stream, later ones
+  // launch it.  Not while stage timing is on or while the caller's stream
+  // is itself being captured.
+  bh_ctx::Key key;
+  memset(&key, 0, sizeof(key));
+  key.pm = pm; key.tg = tg; key.out = out; key.n = N; key.m = M;
+  key.cap_n = c->cap_n; key.cap_m = c->cap_m;
+  key.theta = c->theta; key.G = c->G; key.eps = c->eps;
+  key.bits = c->bits; key.leaf_cap = c->leaf_cap; key.opening = c->opening;
+  key.group = c->group; key.spin = c->spin_limit;
+  bool graph = c->use_graph && !c->timing && c->cap_stream;
+  if (graph) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      graph = false;
   }
-  record(c, 7, s);
-  if (e == cudaSuccess) {
-    WalkArgs a;
-    a.spm = c->spm;
-    a.n = N;
-    a.rec = c->build.rec;
-    a.tpos = self ? c->spm : c->stm;
-    a.tperm = self ? c->sort.idx[fb] : c->sort_t.idx[fbt];
-    a.m = M;
-    a.out = out;
-    a.eps2 = c->eps * c->eps;
-    a.G = c->G;
-    a.self_mode = self ? 1 : 0;
-    a.opening = c->opening;
-    a.group = c->group;
-    a.num_sms = c->num_sms;
-    e = launch_walk(a, c->ctrl, s);
-    c->last_walk = a;
+  bool done = false;
+  if (graph && c->gexec && key == c->gkey) {
+    e = cudaGraphLaunch(c->gexec, s);
+    fb = c->g_fb; fbt = c->g_fbt; walk = c->g_walk;
+    done = true;
+  } else if (graph && c->has_prev && key == c->prev_key) {
+    cudaGraph_t gr = nullptr;
+    cudaError_t ec = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
+    if (ec == cudaSuccess) {
+      ec = enqueue_step(c, pm, N, tg, M, out, self, c->cap_stream, &fb, &fbt, &walk);
+      cudaError_t ee = cudaStreamEndCapture(c->cap_stream, &gr);
+      if (ec == cudaSuccess) ec = ee;
+    }
+    cudaGraphExec_t ex = nullptr;
+    if (ec == cudaSuccess && gr) ec = cudaGraphInstantiate(&ex, gr, 0);
+    if (gr) cudaGraphDestroy(gr);
+    if (ec == cudaSuccess && ex) {
+      if (c->gexec) cudaGraphExecDestroy(c->gexec);
+      c->gexec = ex;
+      c->gkey = key;
+      c->g_fb = fb; c->g_fbt = fbt; c->g_walk = walk;
+      e = cudaGraphLaunch(ex, s);
+      done = true;
+    } else {
+      cudaGetLastError();          // capture unsupported here: run directly
+      c->use_graph = 0;
+    }
   }
-  record(c, 8, s);
+  if (!done) e = enqueue_step(c, pm, N, tg, M, out, self, s, &fb, &fbt, &walk);
+  c->prev_key = key;
+  c->has_prev = true;
+  c->last_walk = walk;
   if (e != cudaSuccess) return cuda_fail(c, e, "launch");
   for (int i = 0; i < BH_NUM_STAGES; ++i) c->stage_ran[i] = true;
   c->stage_ran[BH_STAGE_TARGETS] = !self;

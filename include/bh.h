@@ -60,6 +60,10 @@ typedef struct bh_ctx bh_ctx;
 #define BH_OPT_OPENING       3  /* group opening rule, see BH_OPEN_*         */
 #define BH_OPT_TIMING        4  /* 1: record per-stage CUDA events (default 0) */
 #define BH_OPT_GROUP         5  /* targets per warp group: 32 or 64 (default 64) */
+#define BH_OPT_GRAPH         6  /* 1 (default): a call that repeats the previous
+                                   one exactly (pointers, sizes, parameters,
+                                   options) is captured once as a CUDA graph
+                                   and replayed; 0: always launch kernels   */
 
 #define BH_OPEN_VOTE  0  /* a cell is accepted for a group of targets only if
                             the opening test holds for every target of the

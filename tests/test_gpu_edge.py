@@ -140,3 +140,28 @@ def test_stage_times(B):
     bh.compute(H.to_dev(src))
     t = B.bh_get_stage_times(bh.ctx)
     assert t["traverse"] > 0 and t["sort"] > 0 and t["targets"] == 0.0
+
+
+def test_graph_replay_is_bit_identical(B):
+    """Repeated identical calls are captured once as a CUDA graph and
+    replayed; results must equal plain launches, and changing a parameter
+    must not replay the old graph."""
+    import torch
+    src = H.to_dev(W.plummer(200000, seed=31))
+    plain = B.BarnesHut(theta=0.5, eps=1e-3, graph=0)
+    want = plain.compute(src).clone()
+    want_t6 = None
+    bh = B.BarnesHut(theta=0.5, eps=1e-3)
+    out = torch.empty_like(src)
+    for _ in range(4):                       # direct, capture, replay, replay
+        out.fill_(float("nan"))
+        bh.compute(src, None, out)
+        assert bh.status() == 0
+        assert torch.equal(out, want)
+    bh.set_params(0.6, 1.0, 1e-3)            # new key: no stale replay
+    plain.set_params(0.6, 1.0, 1e-3)
+    want_t6 = plain.compute(src)
+    for _ in range(3):
+        bh.compute(src, None, out)
+        assert torch.equal(out, want_t6)
+    assert not torch.equal(want, want_t6)
