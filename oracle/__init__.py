@@ -18,6 +18,8 @@ the web page section it restates (see the C file's header):
 * ``bh``/``bh_group`` -- GASPHiA page, section 性能瓶颈分析 (opening test
   w_sq/theta_sq < r_sq; the warp vote in the group form).
 * ``direct`` -- GASPHiA page, section 精度与加速比验证 (brute-force double loop).
+* ``leapfrog`` -- kick-drift-kick time stepping with brute-force forces (the
+  pages show an N-body run advanced in time but print no integrator).
 """
 from __future__ import annotations
 
@@ -69,6 +71,8 @@ def lib():
                                    _i32p, _f64p, C.c_double, C.c_double, C.c_double,
                                    C.c_double, _f32p, _vp, C.c_int64, C.c_int64,
                                    C.c_int, _f64p, _vp, _vp]
+        L.orc_leapfrog.argtypes = [_f64p, _f64p, C.c_int64, C.c_double, C.c_double,
+                                   C.c_double, C.c_int64]
         L.orc_num_threads.restype = C.c_int
         L.orc_set_threads.argtypes = [C.c_int]
         _LIB = L
@@ -277,6 +281,16 @@ class OracleBH:
 
     def direct(self, tgt=None, idx=None):
         return direct(self.src, tgt, self.G, self.eps, idx)
+
+
+def leapfrog(pos_mass, vel, G: float = 1.0, eps: float = 0.0, dt: float = 1e-3,
+             nsteps: int = 1):
+    """fp64 kick-drift-kick leapfrog with brute-force forces.  Returns the
+    final (positions+masses (n,4), velocities (n,3)) as fp64 copies."""
+    pos = np.ascontiguousarray(pos_mass, np.float64).copy()
+    v = np.ascontiguousarray(np.asarray(vel, np.float64)[:, :3]).copy()
+    lib().orc_leapfrog(pos, v, pos.shape[0], float(G), float(eps), float(dt), int(nsteps))
+    return pos, v
 
 
 def rel_error(a, ref, floor_frac: float = 1e-3) -> np.ndarray:

@@ -470,3 +470,51 @@ void orc_bh_group(const float *spm, int64_t nnodes, const int32_t *level,
         free(stack);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Leapfrog time integration, kick-drift-kick, with brute-force forces      */
+/* ([T] title video: the 5M-particle galaxy collision is a pure N-body run   */
+/* advanced step by step; the pages do not print an integrator, so the      */
+/* plainest symplectic one is used).  One step:                             */
+/*   v += a(x) dt/2;  x += v dt;  v += a(x) dt/2.                            */
+/* pos (x,y,z,m) and vel (vx,vy,vz) are fp64, updated in place.              */
+/* ------------------------------------------------------------------------ */
+static void accel64(const double *pos, int64_t n, double G, double eps2,
+                    double *acc)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double a[3] = {0, 0, 0};
+        for (int64_t j = 0; j < n; ++j) {
+            if (j == i) continue;
+            double dx = pos[4 * j] - pos[4 * i];
+            double dy = pos[4 * j + 1] - pos[4 * i + 1];
+            double dz = pos[4 * j + 2] - pos[4 * i + 2];
+            double r2 = dx * dx + dy * dy + dz * dz + eps2;
+            if (r2 == 0.0) continue;
+            double inv = 1.0 / sqrt(r2);
+            double w = pos[4 * j + 3] * inv * inv * inv;
+            a[0] += w * dx; a[1] += w * dy; a[2] += w * dz;
+        }
+        for (int k = 0; k < 3; ++k) acc[3 * i + k] = G * a[k];
+    }
+}
+
+void orc_leapfrog(double *pos, double *vel, int64_t n, double G, double eps,
+                  double dt, int64_t nsteps)
+{
+    double *acc = (double *)malloc(sizeof(double) * 3 * (size_t)(n > 0 ? n : 1));
+    double eps2 = eps * eps;
+    accel64(pos, n, G, eps2, acc);
+    for (int64_t s = 0; s < nsteps; ++s) {
+        for (int64_t i = 0; i < n; ++i)
+            for (int k = 0; k < 3; ++k) {
+                vel[3 * i + k] += 0.5 * dt * acc[3 * i + k];
+                pos[4 * i + k] += dt * vel[3 * i + k];
+            }
+        accel64(pos, n, G, eps2, acc);
+        for (int64_t i = 0; i < n; ++i)
+            for (int k = 0; k < 3; ++k) vel[3 * i + k] += 0.5 * dt * acc[3 * i + k];
+    }
+    free(acc);
+}

@@ -352,3 +352,46 @@ def test_theta_table_sanity_band(orc):
         means.append(m)
         assert page[th][3] / 10 < m < page[th][3] * 10
     assert means[0] < means[1] < means[2]
+
+
+# --------------------------------------------------------------------------
+# time integration
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("G", [1.0, 4.0])
+def test_leapfrog_circular_binary(orc, G):
+    """Two masses 1/2 at distance 1: circular orbit about the centre of mass
+    with speed sqrt(G m / (2 d)) = sqrt(G)/2 and period 2*pi*(d/2)/v; after one
+    period the leapfrog returns to the start to O(dt^2) and conserves energy
+    to O(dt^2)."""
+    sp = np.sqrt(G) / 2
+    period = 2 * np.pi * 0.5 / sp
+    p = np.array([[-0.5, 0, 0, 0.5], [0.5, 0, 0, 0.5]], np.float64)
+    v = np.array([[0, -sp, 0], [0, sp, 0]], np.float64)
+    nsteps = 2000
+    dt = period / nsteps
+    pe, ve = orc.leapfrog(p, v, G, 0.0, dt, nsteps)
+    np.testing.assert_allclose(pe[:, :3], p[:, :3], atol=2e-5)
+    np.testing.assert_allclose(ve, v, atol=2e-5 * sp / 0.5)
+    # quarter period: bodies on the y axis
+    pq, _ = orc.leapfrog(p, v, G, 0.0, dt, nsteps // 4)
+    np.testing.assert_allclose(pq[:, :3], [[0, -0.5, 0], [0, 0.5, 0]], atol=2e-5)
+    def energy(pp, vv):
+        d = np.linalg.norm(pp[0, :3] - pp[1, :3])
+        return 0.5 * (pp[:, 3] * (vv * vv).sum(1)).sum() - G * pp[0, 3] * pp[1, 3] / d
+    assert abs(energy(pe, ve) / energy(p, v) - 1.0) < 1e-5
+
+
+def test_leapfrog_time_reversible_and_conserves_momentum(orc):
+    g = W.rng(44)
+    n = 64
+    p = np.zeros((n, 4))
+    p[:, :3] = g.normal(size=(n, 3))
+    p[:, 3] = g.uniform(0.5, 1.5, n) / n
+    v = g.normal(size=(n, 3)) * 0.1
+    p1, v1 = orc.leapfrog(p, v, 1.0, 0.05, 1e-2, 50)
+    mom0 = (p[:, 3:4] * v).sum(0)
+    mom1 = (p1[:, 3:4] * v1).sum(0)
+    assert np.abs(mom1 - mom0).max() < 1e-13
+    p2, v2 = orc.leapfrog(p1, -v1, 1.0, 0.05, 1e-2, 50)      # run it backwards
+    np.testing.assert_allclose(p2[:, :3], p[:, :3], atol=1e-10)
+    np.testing.assert_allclose(-v2, v, atol=1e-10)
