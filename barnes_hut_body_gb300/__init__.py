@@ -25,6 +25,7 @@ BH_OK, BH_EINVAL, BH_ENOMEM, BH_ECUDA, BH_ETIMEOUT, BH_ETREE_OVERFLOW = range(6)
 BH_OPT_KEY_BITS, BH_OPT_LEAF_CAP, BH_OPT_OPENING, BH_OPT_TIMING, BH_OPT_GROUP, BH_OPT_GRAPH = 1, 2, 3, 4, 5, 6
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
 BH_DBG_SPIN_LIMIT = 1
+BH_LF_ACC_VALID = 1
 (BH_EXPORT_CUBE, BH_EXPORT_KEYS, BH_EXPORT_PERM, BH_EXPORT_NODE_COUNT,
  BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM, BH_EXPORT_WALK_STATS) = range(1, 9)
 STAGES = ("bbox", "keys", "sort", "reorder", "build", "com", "targets", "traverse")
@@ -33,7 +34,7 @@ EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
             "bh_set_debug", "bh_compute", "bh_compute_host", "bh_direct",
             "bh_sync_status", "bh_get_stage_times", "bh_get_counters",
             "bh_debug_export", "bh_count_interactions", "bh_direct_static",
-            "bh_last_error")
+            "bh_leapfrog", "bh_last_error")
 
 _lib = None
 
@@ -67,6 +68,7 @@ def lib():
         L.bh_debug_export.argtypes = [vp, i, vp, sz]
         L.bh_count_interactions.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), vp]
         L.bh_direct_static.argtypes = [vp, sz, vp, sz, f, f, vp, vp]
+        L.bh_leapfrog.argtypes = [vp, vp, vp, sz, vp, f, i, i, vp]
         L.bh_last_error.argtypes = [vp]
         L.bh_last_error.restype = C.c_char_p
         for name in EXPORTED:
@@ -173,6 +175,20 @@ def bh_direct_static(pos_mass, targets, acc_pot, G: float = 1.0, eps: float = 0.
     if rc != BH_OK:
         raise BHError(rc, "bh_direct_static failed (bad argument, more than "
                           "262144 targets, or a CUDA error)")
+
+
+def bh_leapfrog(ctx, pos_mass, vel, acc_pot, dt: float, nsteps: int,
+                acc_valid: bool = False, stream=None) -> None:
+    """Kick-drift-kick time stepping with the Barnes-Hut forces, in place on
+    device tensors (n, 4): positions+masses, velocities, accelerations."""
+    p, n = _rows_ptr(pos_mass, "pos_mass")
+    v, nv = _rows_ptr(vel, "vel")
+    a, na = _rows_ptr(acc_pot, "acc_pot")
+    if not (n == nv == na):
+        raise ValueError("pos_mass, vel and acc_pot need the same number of rows")
+    flags = BH_LF_ACC_VALID if acc_valid else 0
+    _check(ctx, lib().bh_leapfrog(ctx, p, v, n, a, float(dt), int(nsteps), flags,
+                                  _stream(pos_mass, stream)))
 
 
 def _host_rows(a, name):

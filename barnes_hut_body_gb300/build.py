@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbh.so")
-SOURCES = ["bh_api.cu", "k_keys_sort.cu", "k_build.cu", "k_walk.cu", "k_direct.cu"]
+SOURCES = ["bh_api.cu", "k_keys_sort.cu", "k_build.cu", "k_walk.cu", "k_direct.cu",
+           "k_integrate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

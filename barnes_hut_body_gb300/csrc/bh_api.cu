@@ -688,6 +688,36 @@ int bh_count_interactions(bh_ctx *c, unsigned int *counts,
   return BH_OK;
 }
 
+int bh_leapfrog(bh_ctx *c, float *pos_mass, float *vel, size_t n,
+                float *acc_pot, float dt, int nsteps, int flags, void *stream) {
+  if (!c) return BH_EINVAL;
+  c->err.clear();
+  int rc;
+  if ((rc = check_rows(c, pos_mass, n, "pos_mass")) != BH_OK) return rc;
+  if ((rc = check_rows(c, vel, n, "vel")) != BH_OK) return rc;
+  if ((rc = check_rows(c, acc_pot, n, "acc_pot")) != BH_OK) return rc;
+  if (!isfinite(dt) || nsteps < 0) return fail(c, BH_EINVAL, "dt must be finite and nsteps >= 0");
+  if (n == 0) return BH_OK;
+  DeviceGuard g(c->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  float4 *pm = reinterpret_cast<float4 *>(pos_mass);
+  float4 *v = reinterpret_cast<float4 *>(vel);
+  float4 *a = reinterpret_cast<float4 *>(acc_pot);
+  const long long N = (long long)n;
+  if (!(flags & BH_LF_ACC_VALID)) {
+    if ((rc = bh_compute(c, pos_mass, n, nullptr, 0, acc_pot, stream)) != BH_OK) return rc;
+  }
+  const float half = 0.5f * dt;
+  for (int k = 0; k < nsteps; ++k) {
+    cudaError_t e = launch_kick_drift(pm, v, a, N, half, dt, c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "kick-drift launch");
+    if ((rc = bh_compute(c, pos_mass, n, nullptr, 0, acc_pot, stream)) != BH_OK) return rc;
+    e = launch_kick(v, a, N, half, c->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(c, e, "kick launch");
+  }
+  return BH_OK;
+}
+
 const char *bh_last_error(const bh_ctx *c) {
   return c ? c->err.c_str() : "null context";
 }

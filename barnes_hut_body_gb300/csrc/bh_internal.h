@@ -136,4 +136,10 @@ cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
                           double *partial, long long partial_cap, float4 *out,
                           int num_sms, cudaStream_t s);
 
+cudaError_t launch_kick_drift(float4 *pm, float4 *vel, const float4 *acc,
+                              long long n, float hk, float dt, int num_sms,
+                              cudaStream_t s);
+cudaError_t launch_kick(float4 *vel, const float4 *acc, long long n, float hk,
+                        int num_sms, cudaStream_t s);
+
 }  // namespace bh

@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--direct", action="store_true",
                     help="time the brute-force kernel (bh_direct) on the workload instead")
+    ap.add_argument("--integrate", action="store_true",
+                    help="time leapfrog simulation steps (bh_leapfrog) instead")
+    ap.add_argument("--dt", type=float, default=1e-4)
     return ap.parse_args()
 
 
@@ -442,6 +445,52 @@ def run_direct(args, rank, local_rank, world):
     return 0
 
 
+def run_integrate(args, rank, local_rank, world):
+    """Leapfrog simulation steps: kick + drift, tree gravity, kick."""
+    import numpy as np
+    import torch
+
+    import barnes_hut_body_gb300 as B
+    import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    src, tgt, G, eps, theta = W.make(args.workload)
+    theta = args.theta if args.theta is not None else theta
+    if tgt is not None:
+        raise SystemExit("--integrate needs a self-gravity workload")
+    n = src.shape[0]
+    d_pm = torch.from_numpy(src).to(device)
+    d_v = torch.zeros((n, 4), dtype=torch.float32, device=device)
+    d_a = torch.zeros((n, 4), dtype=torch.float32, device=device)
+    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank)
+    B.bh_leapfrog(bh.ctx, d_pm, d_v, d_a, args.dt, max(args.warmup, 3))
+    if bh.status() != 0:
+        raise RuntimeError(B.bh_last_error(bh.ctx))
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    B.bh_leapfrog(bh.ctx, d_pm, d_v, d_a, args.dt, args.steps, acc_valid=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    useful = B.bh_count_interactions(bh.ctx)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "leapfrog_steps_per_s", "value": world * 1e3 / ms, "unit": "steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "useful_interactions_per_s": sum_over_ranks(useful, world, device) / (ms / 1e3),
+            "config": dict(workload_config(args.workload, src, tgt, theta, eps), dt=args.dt,
+                           step="kick+drift, tree gravity, kick")}), flush=True)
+    bh.close()
+    return 0
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
@@ -449,6 +498,8 @@ def main():
         return run_reference(args, rank, world)
     if args.direct:
         return run_direct(args, rank, local_rank, world)
+    if args.integrate:
+        return run_integrate(args, rank, local_rank, world)
     return run_ours(args, rank, local_rank, world)
 
 

@@ -193,6 +193,28 @@ int bh_direct_static(const float *pos_mass, size_t n, const float *targets,
                      void *stream);
 
 /*
+ * Leapfrog (kick-drift-kick) time integration of a self-gravitating system
+ * with the forces of bh_compute, the tree rebuilt from the new positions
+ * every step -- the pure N-body run of the GASPHiA page (its galaxy-collision
+ * video); the pages print no integrator, this is the plainest symplectic one:
+ *     v += a dt/2;  x += v dt;  a = bh_compute(x);  v += a dt/2.
+ *
+ *   pos_mass  device, n rows (x,y,z,m); positions updated in place.
+ *   vel       device, n rows (vx,vy,vz,unused); updated in place.
+ *   acc_pot   device, n rows; with BH_LF_ACC_VALID in flags it must hold the
+ *             accelerations at the initial positions (e.g. the output of the
+ *             previous call), otherwise they are computed first.  On return
+ *             it holds (ax,ay,az,phi) at the final positions.
+ *   dt        time step (finite; negative runs backwards); nsteps >= 0.
+ *
+ * Asynchronous on `stream` like bh_compute; parameters and options are the
+ * context's.  Errors of the device stages land in the status word.
+ */
+#define BH_LF_ACC_VALID 1
+int bh_leapfrog(bh_ctx *c, float *pos_mass, float *vel, size_t n,
+                float *acc_pot, float dt, int nsteps, int flags, void *stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word
  * (BH_OK, BH_EINVAL for non-finite input, BH_ETIMEOUT, BH_ETREE_OVERFLOW).
  */
