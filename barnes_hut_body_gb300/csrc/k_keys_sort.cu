@@ -274,142 +274,221 @@ __device__ __forceinline__ unsigned block_excl_scan256(unsigned v,
   return off + x - v;
 }
 
+// ---- TMA bulk copies into shared memory, completion on an mbarrier -------
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long *bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long *bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, unsigned parity) {
+  unsigned ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes,
+                                          unsigned long long *bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+constexpr unsigned kTmaWaitLimit = 1u << 26;   // polls; a bulk copy takes microseconds
+
 struct SortSmem {
-  unsigned long long k[kSortTile];
-  unsigned int v[kSortTile];
+  // Two input stages (keys, then indices).  A stage's data is read into
+  // registers, then the stage is reused to stage the scatter.
+  alignas(128) unsigned long long k[2][kSortTile];
+  alignas(128) unsigned int v[2][kSortTile];
+  unsigned int whist[kSortThreads / 32][256];
+  unsigned int dig_excl[256];
+  unsigned int glob[256];
+  unsigned int gofs[256];
+  unsigned int warp[kSortThreads / 32];
+  alignas(8) unsigned long long bar[2];
+  long long tile[2];
 };
 
+// Persistent pass: each block takes tile tickets in order, one ahead, and
+// prefetches the next tile with TMA bulk copies while it ranks, looks back
+// and scatters the current one.
 template <bool kFirst>
-__global__ void __launch_bounds__(kSortThreads)
+__global__ void __launch_bounds__(kSortThreads, 2)
 sort_pass_kernel(const unsigned long long *__restrict__ kin,
                  const unsigned int *__restrict__ vin,
                  unsigned long long *__restrict__ kout,
-                 unsigned int *__restrict__ vout, long long n, int shift,
-                 const unsigned int *__restrict__ hist,
+                 unsigned int *__restrict__ vout, long long n, long long ntiles,
+                 int shift, const unsigned int *__restrict__ hist,
                  unsigned int *tile_ctr, unsigned long long *status,
                  unsigned int tag_base, DevCtrl *ctrl,
                  unsigned int spin_limit) {
-  __shared__ SortSmem st;
-  __shared__ unsigned int s_whist[kSortThreads / 32][256];
-  __shared__ unsigned int s_dig_excl[256];
-  __shared__ unsigned int s_glob[256];
-  __shared__ unsigned int s_warp[kSortThreads / 32];
-  __shared__ unsigned int s_tile;
-
+  extern __shared__ __align__(128) unsigned char sort_smem_raw[];
+  SortSmem &S = *reinterpret_cast<SortSmem *>(sort_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const unsigned long long tag =
       (unsigned long long)(tag_base + ctrl->keep.epoch * 16u) << 32;
-  if (tid == 0) s_tile = atomicAdd(tile_ctr, 1u);
-  for (int k = tid; k < (kSortThreads / 32) * 256; k += kSortThreads)
-    (&s_whist[0][0])[k] = 0u;
-  // global start of each digit = exclusive scan of this pass's histogram
-  unsigned gofs = block_excl_scan256(hist[tid], s_warp, nullptr);
-  __syncthreads();
-  const long long tile = s_tile;
-  const long long base = tile * kSortTile;
-  const long long wbase = base + (long long)w * (kSortItems * 32);
 
-  unsigned long long key[kSortItems];
-  unsigned int val[kSortItems];
-  unsigned int rnk[kSortItems];
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    long long idx = wbase + i * 32 + lane;
-    bool valid = idx < n;
-    key[i] = valid ? kin[idx] : ~0ull;
-    if (kFirst) val[i] = (unsigned)idx;
-    else val[i] = valid ? vin[idx] : 0u;
+  auto issue = [&](int b, long long t) {
+    // keys (and indices) of tile t into stage b; sizes rounded up to 16
+    // bytes (the buffers are padded past n)
+    const long long base = t * kSortTile;
+    const long long cnt = n - base < kSortTile ? n - base : kSortTile;
+    const unsigned kb = (unsigned)((cnt * 8 + 15) & ~15LL);
+    const unsigned vb = kFirst ? 0u : (unsigned)((cnt * 4 + 15) & ~15LL);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(&S.bar[b], kb + vb);
+    bulk_load(&S.k[b][0], kin + base, kb, &S.bar[b]);
+    if (!kFirst) bulk_load(&S.v[b][0], vin + base, vb, &S.bar[b]);
+  };
+
+  if (tid == 0) {
+    mbar_init(&S.bar[0]);
+    mbar_init(&S.bar[1]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    S.tile[0] = atomicAdd(tile_ctr, 1u);
   }
-  const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    unsigned d = (unsigned)(key[i] >> shift) & 255u;
-    unsigned peers = 0xffffffffu;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      unsigned bit = (d >> b) & 1u;
-      unsigned bal = __ballot_sync(0xffffffffu, bit);
-      peers &= bit ? bal : ~bal;
-    }
-    unsigned before = s_whist[w][d];
-    rnk[i] = before + __popc(peers & lt);
-    __syncwarp();
-    if ((peers & lt) == 0u) s_whist[w][d] = before + __popc(peers);
-    __syncwarp();
-  }
+  // global start of each digit = exclusive scan of this pass's histogram
+  S.gofs[tid] = block_excl_scan256(hist[tid], S.warp, nullptr);
   __syncthreads();
-  // per digit: offsets of the warps within the tile, and the tile's count
-  const unsigned d = tid;
-  unsigned run = 0;
-#pragma unroll
-  for (int k = 0; k < kSortThreads / 32; ++k) {
-    unsigned c = s_whist[k][d];
-    s_whist[k][d] = run;
-    run += c;
-  }
-  const unsigned total = run;
-  // decoupled look-back over the tiles before this one
-  unsigned long long *slot = status + tile * 256 + d;
-  unsigned excl = 0;
-  if (tile == 0) {
-    st_volatile(slot, tag | kFlagPrefix | (unsigned long long)total);
-  } else {
-    st_volatile(slot, tag | kFlagAgg | (unsigned long long)total);
-    // Read a window of predecessors per round trip: when a wave of tiles
-    // starts together, the nearest inclusive prefix can be far back.
-    long long t = tile - 1;
-    unsigned spins = 0;
-    bool done = false;
-    while (t >= 0 && !done) {
-      unsigned long long w[kLookback];
-#pragma unroll
-      for (int k = 0; k < kLookback; ++k)
-        w[k] = (t - k >= 0) ? ld_volatile(status + (t - k) * 256 + d)
-                            : (tag | kFlagPrefix);
-      int used = 0;
-#pragma unroll
-      for (int k = 0; k < kLookback; ++k) {
-        if (done || used < k) break;
-        const unsigned long long sv = w[k];
-        if ((sv & 0xffffffff00000000ull) != tag) break;   // not published yet
-        if (t - k >= 0) excl += (unsigned)(sv & kValMask);
-        used = k + 1;
-        if ((sv & kFlagPrefix) || t - k <= 0) done = true;
-      }
-      t -= used;
-      if (!done && used == 0) {
-        if (++spins > spin_limit) {
+  if (tid == 0 && S.tile[0] < ntiles) issue(0, S.tile[0]);
+  unsigned parity[2] = {0u, 0u};
+  int b = 0;
+  const unsigned lt = (1u << lane) - 1u;
+
+  for (;;) {
+    __syncthreads();                       // previous tile fully written out
+    const long long tile = S.tile[b];
+    if (tile >= ntiles) break;
+    if (tid == 0) {
+      const long long tn = atomicAdd(tile_ctr, 1u);
+      S.tile[b ^ 1] = tn;
+      if (tn < ntiles) issue(b ^ 1, tn);
+    }
+    for (int k = tid; k < (kSortThreads / 32) * 256; k += kSortThreads)
+      (&S.whist[0][0])[k] = 0u;
+    {
+      unsigned spins = 0;
+      while (!mbar_try_wait(&S.bar[b], parity[b])) {
+        if (++spins > kTmaWaitLimit) {
           set_err(ctrl, kErrTimeout);
           break;
         }
-        if (spins > 64) __nanosleep(32);
+      }
+      parity[b] ^= 1u;
+    }
+    const long long base = tile * kSortTile;
+    const int wbase = w * (kSortItems * 32);
+
+    unsigned long long key[kSortItems];
+    unsigned int val[kSortItems];
+    unsigned int rnk[kSortItems];
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+      const int j = wbase + i * 32 + lane;
+      const bool valid = base + j < n;
+      key[i] = valid ? S.k[b][j] : ~0ull;
+      if (kFirst) val[i] = (unsigned)(base + j);
+      else val[i] = valid ? S.v[b][j] : 0u;
+    }
+    __syncthreads();                       // whist zeroed
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+      unsigned d = (unsigned)(key[i] >> shift) & 255u;
+      unsigned peers = 0xffffffffu;
+#pragma unroll
+      for (int bt = 0; bt < 8; ++bt) {
+        unsigned bit = (d >> bt) & 1u;
+        unsigned bal = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? bal : ~bal;
+      }
+      unsigned before = S.whist[w][d];
+      rnk[i] = before + __popc(peers & lt);
+      __syncwarp();
+      if ((peers & lt) == 0u) S.whist[w][d] = before + __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // per digit: offsets of the warps within the tile, and the tile's count
+    const unsigned d = tid;
+    unsigned run = 0;
+#pragma unroll
+    for (int k = 0; k < kSortThreads / 32; ++k) {
+      unsigned c = S.whist[k][d];
+      S.whist[k][d] = run;
+      run += c;
+    }
+    const unsigned total = run;
+    // decoupled look-back over the tiles before this one: publish this
+    // tile's counts, issue the first window of predecessor reads, and do the
+    // block-local scatter (which needs no global offset) while they fly
+    unsigned long long *slot = status + tile * 256 + d;
+    st_volatile(slot, tag | (tile == 0 ? kFlagPrefix : kFlagAgg) |
+                          (unsigned long long)total);
+    long long t = tile - 1;
+    unsigned long long wv[kLookback];
+#pragma unroll
+    for (int k = 0; k < kLookback; ++k)
+      wv[k] = (t - k >= 0) ? ld_volatile(status + (t - k) * 256 + d) : (tag | kFlagPrefix);
+    S.dig_excl[d] = block_excl_scan256(total, S.warp, nullptr);
+    __syncthreads();
+    // scatter into the stage in digit order
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {
+      unsigned dd = (unsigned)(key[i] >> shift) & 255u;
+      unsigned pos = S.dig_excl[dd] + S.whist[w][dd] + rnk[i];
+      S.k[b][pos] = key[i];
+      S.v[b][pos] = val[i];
+    }
+    unsigned excl = 0;
+    if (tile > 0) {
+      unsigned spins = 0;
+      bool done = false;
+      for (;;) {
+        int used = 0;
+#pragma unroll
+        for (int k = 0; k < kLookback; ++k) {
+          if (done || used < k) break;
+          const unsigned long long sv = wv[k];
+          if ((sv & 0xffffffff00000000ull) != tag) break;   // not published yet
+          if (t - k >= 0) excl += (unsigned)(sv & kValMask);
+          used = k + 1;
+          if ((sv & kFlagPrefix) || t - k <= 0) done = true;
+        }
+        t -= used;
+        if (done || t < 0) break;
+        if (used == 0) {
+          if (++spins > spin_limit) {
+            set_err(ctrl, kErrTimeout);
+            break;
+          }
+          if (spins > 64) __nanosleep(32);
+        }
+#pragma unroll
+        for (int k = 0; k < kLookback; ++k)
+          wv[k] = (t - k >= 0) ? ld_volatile(status + (t - k) * 256 + d) : (tag | kFlagPrefix);
+      }
+      st_volatile(slot, tag | kFlagPrefix |
+                            ((unsigned long long)(excl + total) & kValMask));
+    }
+    S.glob[d] = S.gofs[d] + excl;
+    __syncthreads();
+    // write out: consecutive slots of one digit go to consecutive addresses
+    const long long nvalid = n - base < kSortTile ? n - base : kSortTile;
+    for (int j = tid; j < nvalid; j += kSortThreads) {
+      unsigned long long k = S.k[b][j];
+      unsigned dd = (unsigned)(k >> shift) & 255u;
+      unsigned long long g = (unsigned long long)S.glob[dd] + (j - S.dig_excl[dd]);
+      if (g < (unsigned long long)n) {
+        kout[g] = k;
+        vout[g] = S.v[b][j];
       }
     }
-    st_volatile(slot, tag | kFlagPrefix |
-                          ((unsigned long long)(excl + total) & kValMask));
-  }
-  s_glob[d] = gofs + excl;
-  s_dig_excl[d] = block_excl_scan256(total, s_warp, nullptr);
-  __syncthreads();
-  // scatter into shared memory in digit order
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    unsigned dd = (unsigned)(key[i] >> shift) & 255u;
-    unsigned pos = s_dig_excl[dd] + s_whist[w][dd] + rnk[i];
-    st.k[pos] = key[i];
-    st.v[pos] = val[i];
-  }
-  __syncthreads();
-  // write out: consecutive slots of one digit go to consecutive addresses
-  const long long nvalid = n - base < kSortTile ? n - base : kSortTile;
-  for (int j = tid; j < nvalid; j += kSortThreads) {
-    unsigned long long k = st.k[j];
-    unsigned dd = (unsigned)(k >> shift) & 255u;
-    unsigned long long g = (unsigned long long)s_glob[dd] + (j - s_dig_excl[dd]);
-    if (g < (unsigned long long)n) {
-      kout[g] = k;
-      vout[g] = st.v[j];
-    }
+    b ^= 1;
   }
 }
 
@@ -461,33 +540,33 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
                         int which, unsigned spin_limit, int *final_buf,
                         cudaStream_t s) {
-  static bool carveout = false;
-  if (!carveout) {
-    // ~47 KB of shared memory per tile: ask for the largest shared carveout
-    // so that more than two tiles fit on an SM.
+  static bool attr = false;
+  const size_t smem = sizeof(SortSmem);
+  if (!attr) {
     cudaFuncSetAttribute(sort_pass_kernel<true>,
-                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(sort_pass_kernel<false>,
-                         cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    carveout = true;
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr = true;
   }
   const int passes = (3 * bits + 7) / 8;
   const long long tiles = (n + kSortTile - 1) / kSortTile;
   if (tiles > b.cap_tiles) return cudaErrorInvalidValue;
+  long long grid = (long long)sm_count() * 2;
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
   int cur = 0;
   for (int p = 0; p < passes; ++p) {
     const unsigned *hist = &ctrl->step.hist[which][p][0];
     unsigned *ctr = &ctrl->step.tile_ctr[which][p];
     unsigned tag = (unsigned)(which * 8 + p);
     if (p == 0)
-      sort_pass_kernel<true><<<(unsigned)tiles, kSortThreads, 0, s>>>(
-          b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, 8 * p,
+      sort_pass_kernel<true><<<(unsigned)grid, kSortThreads, smem, s>>>(
+          b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
     else
-      sort_pass_kernel<false><<<(unsigned)tiles, kSortThreads, 0, s>>>(
-          b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, 8 * p,
+      sort_pass_kernel<false><<<(unsigned)grid, kSortThreads, smem, s>>>(
+          b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
     cur ^= 1;
   }
