@@ -18,6 +18,10 @@ the web page section it restates (see the C file's header):
 * ``bh``/``bh_group`` -- GASPHiA page, section 性能瓶颈分析 (opening test
   w_sq/theta_sq < r_sq; the warp vote in the group form).
 * ``direct`` -- GASPHiA page, section 精度与加速比验证 (brute-force double loop).
+* ``sbh`` -- stochastic Barnes-Hut ("Stochastic Barnes-Hut Approximation for
+  Fast Summation on the GPU" page, section 方法: telescoping path sums, Russian
+  roulette on the path length, stratification), with ``philox4x64`` as its
+  counter-based random numbers.
 * ``leapfrog`` -- kick-drift-kick time stepping with brute-force forces (the
   pages show an N-body run advanced in time but print no integrator).
 """
@@ -71,6 +75,11 @@ def lib():
                                    _i32p, _f64p, C.c_double, C.c_double, C.c_double,
                                    C.c_double, _f32p, _vp, C.c_int64, C.c_int64,
                                    C.c_int, _f64p, _vp, _vp]
+        L.orc_philox4x64.argtypes = [_u64p, _u64p, _u64p]
+        L.orc_sbh.argtypes = [_f32p, C.c_int64, _i32p, _i64p, _i64p, _i64p, _i32p,
+                              _f64p, C.c_float, C.c_double, C.c_double, _f32p, _vp,
+                              _i64p, C.c_int64, C.c_uint64, C.c_int, C.c_int, _f64p,
+                              _i64p, _f64p, _f64p]
         L.orc_leapfrog.argtypes = [_f64p, _f64p, C.c_int64, C.c_double, C.c_double,
                                    C.c_double, C.c_int64]
         L.orc_num_threads.restype = C.c_int
@@ -281,6 +290,45 @@ class OracleBH:
 
     def direct(self, tgt=None, idx=None):
         return direct(self.src, tgt, self.G, self.eps, idx)
+
+    def sbh(self, tgt=None, rows=None, seed=0, strata_level=2, samples=1,
+            group=32):
+        """Stochastic Barnes-Hut estimate for target rows ``rows`` (original
+        indices, default all), in that order.  Queries share random numbers
+        within a group of ``group`` consecutive Morton-ordered targets.
+        Returns (out[k,4], terms[k], absacc[k], abspot[k])."""
+        order = self.target_order(tgt)
+        k_all = order.shape[0]
+        gpos = np.empty(k_all, np.int64)
+        gpos[order] = np.arange(k_all) // group
+        rr = np.arange(k_all) if rows is None else np.asarray(rows, np.int64)
+        if tgt is None:
+            pos = np.ascontiguousarray(self.src[rr])
+            selfj = np.ascontiguousarray(self.rank[rr])
+        else:
+            pos = np.ascontiguousarray(_rows(tgt)[rr])
+            selfj = None
+        k = pos.shape[0]
+        grp = np.ascontiguousarray(gpos[rr])
+        out = np.zeros((k, 4), np.float64)
+        terms = np.zeros(k, np.int64)
+        aa = np.zeros(k, np.float64)
+        ap = np.zeros(k, np.float64)
+        t = self.tree
+        lib().orc_sbh(self.spm, self.nnodes, t["level"], t["first"], t["count"],
+                      t["child"], t["nchild"], self.com, float(self.cube[3]), self.G,
+                      self.eps, pos, _ptr(selfj), grp, k, int(seed) & (2**64 - 1),
+                      int(strata_level), int(samples), out, terms, aa, ap)
+        return out, terms, aa, ap
+
+
+def philox4x64(counter, key) -> np.ndarray:
+    """Philox4x64-10 block for a 4-word counter and 2-word key (uint64)."""
+    c = np.ascontiguousarray(counter, np.uint64)
+    k = np.ascontiguousarray(key, np.uint64)
+    out = np.zeros(4, np.uint64)
+    lib().orc_philox4x64(c, k, out)
+    return out
 
 
 def leapfrog(pos_mass, vel, G: float = 1.0, eps: float = 0.0, dt: float = 1e-3,

@@ -518,3 +518,180 @@ void orc_leapfrog(double *pos, double *vel, int64_t n, double G, double eps,
     }
     free(acc);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x64-10, the counter-based generator of Salmon, Moraes, Dror and    */
+/* Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011).  Each of   */
+/* ten rounds forms the 128-bit products of words 0 and 2 with the two round */
+/* multipliers, builds the new words from the high halves xor the odd words  */
+/* xor the key and from the low halves, then adds the two Weyl constants to  */
+/* the key.                                                                  */
+/* ------------------------------------------------------------------------ */
+void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        unsigned __int128 p0 = (unsigned __int128)0xD2E7470EE14C6C93ull * x0;
+        unsigned __int128 p1 = (unsigned __int128)0xCA5A826395121157ull * x2;
+        uint64_t y0 = (uint64_t)(p1 >> 64) ^ x1 ^ k0;
+        uint64_t y1 = (uint64_t)p1;
+        uint64_t y2 = (uint64_t)(p0 >> 64) ^ x3 ^ k1;
+        uint64_t y3 = (uint64_t)p0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += 0x9E3779B97F4A7C15ull;
+        k1 += 0xBB67AE8584CAA73Bull;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stochastic Barnes-Hut ([P] "Stochastic Barnes-Hut Approximation for Fast  */
+/* Summation on the GPU", section 方法, 关键设计 1-4).  The exact sum is a     */
+/* telescoping sum along each source's root-to-leaf path; one path per       */
+/* stratum is drawn (index I uniform among the stratum's particles), its     */
+/* length cut by Russian roulette, and each refinement step that survives is */
+/* weighted by 1 / (P(I in T) * P(reach the step)), which keeps the estimate  */
+/* unbiased.  Refining a cell T replaces its monopole by its children's:     */
+/*   Delta_T(q) = sum_{c child of T} m_c f(p_c, q) - m_T f(p_T, q)            */
+/* Readings where the page is silent or written for another tree:            */
+/*  - tree: the canonical octree above (2 children per axis, not the page's  */
+/*    4); strata are its cells at level s plus the leaves above level s,     */
+/*    standing in for the children of the page's root;                       */
+/*  - a leaf's children are its particles (the self particle contributes 0);*/
+/*    a particle's size is half the edge of its leaf;                       */
+/*  - far-field ratio beta(T) = |q - p_T| / w_T, p_T the centre of mass, w_T */
+/*    the cell edge; continue from T to the path child c with probability   */
+/*    p = min(1, max(1, beta(T)) / beta(c)), 1 where beta(c) = 0; the       */
+/*    decision u < p is taken in fp32 (the page computes in single          */
+/*    precision), everything else in fp64;                                  */
+/*  - random numbers: Philox4x64-10, key (seed, 0), counter (group, stratum, */
+/*    sample, block).  Block 0 word 0 gives I = floor(o * n_R / 2^64);       */
+/*    roulette step k uses block 1 + k/4, word k%4, as u = (o >> 40) 2^-24.  */
+/*    Queries of one group (32 consecutive Morton-ordered queries, one warp) */
+/*    share every random number, as the page shares seeds across a warp;     */
+/*  - S samples per stratum are averaged.                                    */
+/* grp[r]: group of target row r.  out: k rows (ax,ay,az,phi)*G.  terms:     */
+/* kernel evaluations per row.  absacc / abspot (may be NULL): G * sum of    */
+/* |weight * term| of the acceleration / potential, the rounding scale.      */
+/* ------------------------------------------------------------------------ */
+static float beta32(const float *q, const float *p, float w)
+{
+    float dx = q[0] - p[0], dy = q[1] - p[1], dz = q[2] - p[2];
+    float d2 = dx * dx + dy * dy;
+    d2 = d2 + dz * dz;
+    return sqrtf(d2) / w;
+}
+
+static float continue_prob(float beta_t, float beta_c)
+{
+    if (!(beta_c > 0.0f)) return 1.0f;
+    float p = fmaxf(1.0f, beta_t) / beta_c;
+    return p < 1.0f ? p : 1.0f;
+}
+
+/* one weighted softened term of mass m at s on target x */
+static int64_t wterm(const double *x, double sx, double sy, double sz, double m,
+                     double wgt, double eps2, double *acc, double *aa, double *ap)
+{
+    double t[4] = {0, 0, 0, 0};
+    pair_term(x, sx, sy, sz, m, eps2, t);
+    for (int a = 0; a < 4; ++a) acc[a] += wgt * t[a];
+    *aa += fabs(wgt) * pair_mag(x, sx, sy, sz, m, eps2);
+    *ap += fabs(wgt * t[3]);
+    return 1;
+}
+
+void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
+             const int64_t *first, const int64_t *count, const int64_t *child,
+             const int32_t *nchild, const double *com, float L, double G,
+             double eps, const float *tgt_pos, const int64_t *self_j,
+             const int64_t *grp, int64_t k, uint64_t seed, int strata_level,
+             int samples, double *out, int64_t *terms, double *absacc,
+             double *abspot)
+{
+    double eps2 = eps * eps;
+    /* strata, in node order */
+    int64_t ns = 0;
+    int64_t *strata = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nnodes + 1));
+    for (int64_t c = 0; c < nnodes; ++c)
+        if (level[c] == strata_level || (level[c] < strata_level && child[c] < 0))
+            strata[ns++] = c;
+    const uint64_t key[2] = {seed, 0};
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < k; ++r) {
+        const float qf[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
+        const double x[3] = {qf[0], qf[1], qf[2]};
+        const int64_t self = self_j ? self_j[r] : -1;
+        double acc[4] = {0, 0, 0, 0}, aa = 0.0, ap = 0.0;
+        int64_t nterm = 0;
+        for (int64_t si = 0; si < ns; ++si) {
+            const int64_t R = strata[si];
+            const double *cR = com + 4 * R;
+            /* the stratum's monopole */
+            nterm += wterm(x, cR[0], cR[1], cR[2], cR[3], 1.0, eps2, acc, &aa, &ap);
+            for (int s = 0; s < samples; ++s) {
+                uint64_t ctr[4] = {(uint64_t)grp[r], (uint64_t)si, (uint64_t)s, 0};
+                uint64_t o[4], ou[4];
+                orc_philox4x64(ctr, key, o);
+                int64_t I = (int64_t)(((unsigned __int128)o[0] *
+                                       (unsigned __int128)(uint64_t)count[R]) >> 64);
+                int64_t J = first[R] + I;        /* sorted index of the path's particle */
+                int64_t T = R;
+                double P = 1.0;
+                for (int step = 0;; ++step) {
+                    const int leaf = child[T] < 0;
+                    const float wT = ldexpf(L, -level[T]);
+                    const float wc = ldexpf(L, -(level[T] + 1));
+                    const float pT[3] = {(float)com[4 * T], (float)com[4 * T + 1],
+                                         (float)com[4 * T + 2]};
+                    int64_t c = -1;              /* path child node (internal T) */
+                    float pc[3];
+                    if (leaf) {
+                        for (int a = 0; a < 3; ++a) pc[a] = spm[4 * J + a];
+                    } else {
+                        for (int q = 0; q < nchild[T]; ++q) {
+                            int64_t cc = child[T] + q;
+                            if (first[cc] <= J && J < first[cc] + count[cc]) c = cc;
+                        }
+                        for (int a = 0; a < 3; ++a) pc[a] = (float)com[4 * c + a];
+                    }
+                    float p = continue_prob(beta32(qf, pT, wT), beta32(qf, pc, wc));
+                    if (step % 4 == 0) {
+                        ctr[3] = (uint64_t)(1 + step / 4);
+                        orc_philox4x64(ctr, key, ou);
+                    }
+                    float u = (float)(ou[step % 4] >> 40) * 0x1p-24f;
+                    if (!(u < p)) break;         /* roulette ends the path */
+                    P *= (double)p;
+                    double wgt = ((double)count[R] / (double)count[T]) / P / samples;
+                    /* Delta_T: children's monopoles minus T's own */
+                    if (leaf) {
+                        for (int64_t j = first[T]; j < first[T] + count[T]; ++j) {
+                            if (j == self) continue;
+                            const float *pj = spm + 4 * j;
+                            nterm += wterm(x, pj[0], pj[1], pj[2], pj[3], wgt, eps2,
+                                           acc, &aa, &ap);
+                        }
+                    } else {
+                        for (int q = 0; q < nchild[T]; ++q) {
+                            const double *cc = com + 4 * (child[T] + q);
+                            nterm += wterm(x, cc[0], cc[1], cc[2], cc[3], wgt, eps2,
+                                           acc, &aa, &ap);
+                        }
+                    }
+                    const double *cT = com + 4 * T;
+                    nterm += wterm(x, cT[0], cT[1], cT[2], cT[3], -wgt, eps2, acc,
+                                   &aa, &ap);
+                    if (leaf) break;
+                    T = c;
+                }
+            }
+        }
+        for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[a];
+        if (terms) terms[r] = nterm;
+        if (absacc) absacc[r] = fabs(G) * aa;
+        if (abspot) abspot[r] = fabs(G) * ap;
+    }
+    free(strata);
+}
