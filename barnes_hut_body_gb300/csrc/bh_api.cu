@@ -27,6 +27,10 @@ struct bh_ctx {
   int num_sms = 1;
   float theta = 0.5f, G = 1.f, eps = 0.f;
   int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
+  int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
+  unsigned long long seed = 0;
+  int *strata = nullptr;
+  int strata_cap = 0;
   unsigned spin_limit = 1u << 22;
   std::string err;
 
@@ -62,6 +66,8 @@ struct bh_ctx {
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
+    int estimator, samples, strata_level;
+    unsigned long long seed;
     bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
   };
   int use_graph = 1;
@@ -260,7 +266,29 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   a.opening = c->opening;
   a.group = c->group;
   a.num_sms = c->num_sms;
-  if (e == cudaSuccess) e = launch_walk(a, c->ctrl, s);
+  if (c->estimator == BH_EST_STOCHASTIC) {
+    SbhArgs b;
+    b.spm = c->spm;
+    b.n = N;
+    b.rec = c->build.rec;
+    b.topo = c->build.topo;
+    b.nodes = c->build.cap_nodes;
+    b.strata = c->strata;
+    b.tpos = a.tpos;
+    b.tperm = a.tperm;
+    b.m = M;
+    b.out = out;
+    b.eps2 = a.eps2;
+    b.G = c->G;
+    b.self_mode = a.self_mode;
+    b.strata_level = c->strata_level;
+    b.samples = c->samples;
+    b.num_sms = c->num_sms;
+    b.seed = c->seed;
+    if (e == cudaSuccess) e = launch_sbh(b, c->strata, c->strata_cap, c->ctrl, s);
+  } else if (e == cudaSuccess) {
+    e = launch_walk(a, c->ctrl, s);
+  }
   record(c, 8, s);
   *fb_out = fb;
   *fbt_out = fbt;
@@ -309,6 +337,7 @@ int bh_destroy(bh_ctx *c) {
     free_sources(c);
     free_targets(c);
     free_dev(c->status);
+    free_dev(c->strata);
     free_dev(c->ctrl);
     free_dev(c->partials);
     free_dev(c->dpartial);
@@ -360,6 +389,22 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       if (v != 32 && v != 64) return fail(c, BH_EINVAL, "group must be 32 or 64");
       c->group = (int)v;
       return BH_OK;
+    case BH_OPT_ESTIMATOR:
+      if (v != BH_EST_BARNES_HUT && v != BH_EST_STOCHASTIC)
+        return fail(c, BH_EINVAL, "unknown estimator");
+      c->estimator = (int)v;
+      return BH_OK;
+    case BH_OPT_SEED:
+      c->seed = (unsigned long long)v;
+      return BH_OK;
+    case BH_OPT_SAMPLES:
+      if (v < 1 || v > 1024) return fail(c, BH_EINVAL, "samples must be in 1..1024");
+      c->samples = (int)v;
+      return BH_OK;
+    case BH_OPT_STRATA_LEVEL:
+      if (v < 0 || v > 6) return fail(c, BH_EINVAL, "strata level must be in 0..6");
+      c->strata_level = (int)v;
+      return BH_OK;
     default:
       return fail(c, BH_EINVAL, "unknown option");
   }
@@ -395,6 +440,11 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   }
   if ((rc = ensure_sources(c, N)) != BH_OK) return rc;
   if (!self && (rc = ensure_targets(c, M)) != BH_OK) return rc;
+  if (c->estimator == BH_EST_STOCHASTIC && !c->strata) {
+    // strata of level s <= 6 number at most 8^6
+    if (!alloc_dev(c->strata, 1LL << 18)) return fail(c, BH_ENOMEM, "strata list");
+    c->strata_cap = 1 << 18;
+  }
 
   const float4 *pm = reinterpret_cast<const float4 *>(pos_mass);
   const float4 *tg = reinterpret_cast<const float4 *>(targets);
@@ -415,6 +465,8 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.theta = c->theta; key.G = c->G; key.eps = c->eps;
   key.bits = c->bits; key.leaf_cap = c->leaf_cap; key.opening = c->opening;
   key.group = c->group; key.spin = c->spin_limit;
+  key.estimator = c->estimator; key.samples = c->samples;
+  key.strata_level = c->strata_level; key.seed = c->seed;
   bool graph = c->use_graph && !c->timing && c->cap_stream;
   if (graph) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -36,7 +36,7 @@ struct StepCtrl {
   unsigned int tile_ctr[2][kMaxPasses];    // radix tile tickets per pass
   unsigned int bbox_done[2];               // blocks finished in the bbox pass
   unsigned int work_ctr;                   // traversal group tickets
-  unsigned int pad0;
+  int strata;                              // stochastic walk: strata found
   unsigned long long executed;             // source terms evaluated
   unsigned long long groups;               // groups walked
   unsigned long long useful;               // per-target interaction count
@@ -128,6 +128,28 @@ struct WalkArgs {
   int num_sms;
 };
 cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s);
+
+// Stochastic Barnes-Hut walk (one warp per 32 Morton-ordered queries).
+struct SbhArgs {
+  const float4 *spm;          // sorted sources
+  long long n;
+  const NodeRec *rec;
+  const int4 *topo;           // (first, end, first child, child end) per node
+  long long nodes;            // node pool capacity (bounds every node index)
+  const int *strata;          // filled by the strata pass
+  const float4 *tpos;         // targets in walk order
+  const unsigned int *tperm;  // walk order -> caller index
+  long long m;
+  float4 *out;                // caller order
+  float eps2, G;
+  int self_mode;
+  int strata_level;
+  int samples;
+  int num_sms;
+  unsigned long long seed;
+};
+cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
+                       DevCtrl *ctrl, cudaStream_t s);
 cudaError_t launch_count(const WalkArgs &a, unsigned int *counts, DevCtrl *ctrl,
                          cudaStream_t s);
 

@@ -1,0 +1,312 @@
+// Stochastic Barnes-Hut ("Stochastic Barnes-Hut Approximation for Fast
+// Summation on the GPU", section 方法, key designs 1-4).
+//
+// The exact sum over the sources is a telescoping sum along each source's
+// root-to-leaf path: refining a cell T replaces its monopole by its children's,
+//   Delta_T(q) = sum_{c child of T} m_c f(p_c, q) - m_T f(p_T, q).
+// Per stratum R (the octree's cells at level s, plus leaves above s) a query
+// takes R's monopole and one random path per sample: the path index I is
+// uniform among R's particles, each step continues with probability
+// p = min(1, max(1, beta_T) / beta_c) (beta = distance to the centre of mass
+// over the cell edge; a leaf's children are its particles, of size half the
+// leaf edge), and a surviving step adds Delta_T * (n_R / n_T) / P(reach it).
+//
+// GPU layout: one warp per group of 32 consecutive Morton-ordered queries,
+// one query per lane.  The random numbers belong to the group (the page
+// shares seeds across a warp), so every lane follows the same path I and
+// the node loads are warp-uniform; lanes differ only in where their roulette
+// stops.  Random numbers: Philox4x64-10 with key (seed, 0) and counter
+// (group, stratum, sample, block); block 0 word 0 gives I, roulette step k
+// reads block 1 + k/4, word k%4.  The 32 lanes compute the 8 blocks of 4
+// (stratum, sample) pairs at once.  The roulette decision u < p is taken in
+// fp32 with every operation rounded as written (no contraction), so it
+// depends only on the inputs and the tree.
+#include <climits>
+
+#include "bh_internal.h"
+
+namespace bh {
+namespace {
+
+constexpr int kSbhThreads = 256;
+constexpr int kRngBlocks = 8;                       // Philox blocks per path
+constexpr int kMaxSteps = 4 * (kRngBlocks - 1);     // 28 >= 22 steps of any path
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
+  atomicCAS(&c->keep.err, 0u, code);
+}
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC 2011).
+__device__ __forceinline__ void philox4x64_10(unsigned long long c0,
+                                              unsigned long long c1,
+                                              unsigned long long c2,
+                                              unsigned long long c3,
+                                              unsigned long long k0,
+                                              unsigned long long k1,
+                                              unsigned long long o[4]) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long h0 = __umul64hi(0xD2E7470EE14C6C93ull, c0);
+    const unsigned long long l0 = 0xD2E7470EE14C6C93ull * c0;
+    const unsigned long long h1 = __umul64hi(0xCA5A826395121157ull, c2);
+    const unsigned long long l1 = 0xCA5A826395121157ull * c2;
+    c0 = h1 ^ c1 ^ k0;
+    c1 = l1;
+    c2 = h0 ^ c3 ^ k1;
+    c3 = l0;
+    k0 += 0x9E3779B97F4A7C15ull;
+    k1 += 0xBB67AE8584CAA73Bull;
+  }
+  o[0] = c0; o[1] = c1; o[2] = c2; o[3] = c3;
+}
+
+__device__ __forceinline__ unsigned long long shfl64(unsigned long long v, int src) {
+  unsigned lo = __shfl_sync(kFull, (unsigned)v, src);
+  unsigned hi = __shfl_sync(kFull, (unsigned)(v >> 32), src);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// beta = |q - p| / w, each operation rounded to fp32 in this order.
+__device__ __forceinline__ float beta_rn(const float4 &q, float px, float py,
+                                         float pz, float w) {
+  const float dx = __fsub_rn(q.x, px), dy = __fsub_rn(q.y, py),
+              dz = __fsub_rn(q.z, pz);
+  float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
+  d2 = __fadd_rn(d2, __fmul_rn(dz, dz));
+  return __fdiv_rn(__fsqrt_rn(d2), w);
+}
+
+__device__ __forceinline__ float continue_prob(float bt, float bc) {
+  if (!(bc > 0.f)) return 1.f;
+  const float p = __fdiv_rn(fmaxf(1.f, bt), bc);
+  return p < 1.f ? p : 1.f;
+}
+
+// w = L * 2^-level, exact for the levels of a 21-bit tree.
+__device__ __forceinline__ float edge(float L, int level) {
+  return L * __int_as_float((127 - level) << 23);
+}
+
+// One softened monopole term of mass m at s on query q: (a, phi) / G.
+__device__ __forceinline__ float4 mono(const float4 &q, float sx, float sy,
+                                       float sz, float m, float eps2) {
+  const float dx = sx - q.x, dy = sy - q.y, dz = sz - q.z;
+  const float r2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, eps2)));
+  const float inv = r2 > 0.f ? rsqrtf(r2) : 0.f;
+  const float mi = m * inv;
+  const float mi3 = mi * inv * inv;
+  return make_float4(mi3 * dx, mi3 * dy, mi3 * dz, -mi);
+}
+
+__device__ __forceinline__ void axpy(float4 &acc, float w, const float4 &t) {
+  acc.x = fmaf(w, t.x, acc.x);
+  acc.y = fmaf(w, t.y, acc.y);
+  acc.z = fmaf(w, t.z, acc.z);
+  acc.w = fmaf(w, t.w, acc.w);
+}
+
+// Strata: nodes at level s and leaves above it, in node order.  Levels
+// ascend along the breadth-first node array, so they all lie in the first
+// sum_{l <= s} level_total[l] nodes.  One block, ordered compaction.
+__global__ void __launch_bounds__(1024) strata_kernel(const NodeRec *__restrict__ rec,
+                                                      long long nodes_cap, int s, int cap,
+                                                      int *strata, DevCtrl *ctrl) {
+  __shared__ unsigned warp_cnt[32];
+  __shared__ int base_s;
+  long long prefix = 0;
+  for (int l = 0; l <= s && l < kMaxLevels; ++l) prefix += ctrl->step.level_total[l];
+  if (prefix > nodes_cap) prefix = nodes_cap;       // never read past the pool
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) base_s = 0;
+  __syncthreads();
+  for (long long c0 = 0; c0 < prefix; c0 += blockDim.x) {
+    const long long c = c0 + threadIdx.x;
+    bool take = false;
+    if (c < prefix) {
+      const int fl = rec[c].flags;
+      const int lv = (fl >> 8) & 255;
+      take = lv == s || (lv < s && (fl & 1));
+    }
+    const unsigned bal = __ballot_sync(kFull, take);
+    if (lane == 0) warp_cnt[w] = __popc(bal);
+    __syncthreads();
+    int off = base_s;
+    for (int k = 0; k < w; ++k) off += warp_cnt[k];
+    const int pos = off + __popc(bal & ((1u << lane) - 1u));
+    if (take) {
+      if (pos < cap) strata[pos] = (int)c;
+      else set_err(ctrl, kErrOverflow);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int k = 0; k < (int)(blockDim.x >> 5); ++k) tot += warp_cnt[k];
+      base_s += tot;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) ctrl->step.strata = base_s < cap ? base_s : cap;
+}
+
+template <bool kSelf>
+__global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ctrl) {
+  const int lane = threadIdx.x & 31;
+  const float L = ctrl->keep.cube[0].w;
+  const long long ns = ctrl->step.strata;
+  const long long S = a.samples;
+  const long long npairs = ns * S;
+  const long long ngroups = (a.m + 31) / 32;
+  const float inv_s = 1.f / (float)S;
+  unsigned long long useful = 0, groups = 0;
+  for (;;) {
+    unsigned g = 0;
+    if (lane == 0) g = atomicAdd(&ctrl->step.work_ctr, 1u);
+    g = __shfl_sync(kFull, g, 0);
+    if ((long long)g >= ngroups) break;
+    ++groups;
+    const long long qi = (long long)g * 32 + lane;
+    const bool valid = qi < a.m;
+    const float4 q = a.tpos[valid ? qi : a.m - 1];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    unsigned nterm = 0;
+    for (long long t0 = 0; t0 < npairs; t0 += 4) {
+      // lane 8j + b: block b of pair t0 + j
+      unsigned long long o[4];
+      {
+        const long long t = t0 + (lane >> 3);
+        const long long r = t / S, smp = t - r * S;
+        philox4x64_10((unsigned long long)g, (unsigned long long)r,
+                      (unsigned long long)smp, (unsigned long long)(lane & 7),
+                      a.seed, 0ull, o);
+      }
+      const int jn = npairs - t0 < 4 ? (int)(npairs - t0) : 4;
+      for (int j = 0; j < jn; ++j) {
+        const long long t = t0 + j;
+        const long long r = t / S, smp = t - r * S;
+        const int R = a.strata[r];
+        const NodeRec recR = a.rec[R];
+        const int4 topR = a.topo[R];
+        const long long nR = (long long)topR.y - topR.x;
+        float4 fpar = mono(q, recR.com.x, recR.com.y, recR.com.z, recR.com.w, a.eps2);
+        if (smp == 0) {                      // the stratum's monopole, once
+          axpy(acc, 1.f, fpar);
+          nterm += 1;
+        }
+        const unsigned long long w0 = shfl64(o[0], 8 * j);
+        long long J = topR.x + (long long)__umul64hi(w0, (unsigned long long)nR);
+        if (J < 0 || J >= a.n) J = 0;         // only a corrupt tree gets here
+        NodeRec rT = recR;
+        long long nT = nR;
+        float P = 1.f;
+        bool active = valid;
+        for (int k = 0; k < kMaxSteps; ++k) {
+          const bool leaf = rT.flags & 1;
+          const int lv = (rT.flags >> 8) & 255;
+          const float wT = edge(L, lv), wc = edge(L, lv + 1);
+          float cx, cy, cz;
+          int cidx = -1;
+          if (leaf) {
+            const float4 pj = a.spm[J];
+            cx = pj.x; cy = pj.y; cz = pj.z;
+          } else {
+            // the path child: the last child whose first particle is <= J
+            const int nc = rT.count < 8 ? rT.count : 8;
+            const bool in = lane < nc && rT.link >= 0 && rT.link + lane < a.nodes;
+            const int f = in ? a.topo[rT.link + lane].x : INT_MAX;
+            const unsigned bal = __ballot_sync(kFull, (long long)f <= J);
+            if (bal == 0u) break;             // only a corrupt tree gets here
+            cidx = rT.link + 31 - __clz(bal);
+            const float4 cc = a.rec[cidx].com;
+            cx = cc.x; cy = cc.y; cz = cc.z;
+          }
+          const float p = continue_prob(beta_rn(q, rT.com.x, rT.com.y, rT.com.z, wT),
+                                        beta_rn(q, cx, cy, cz, wc));
+          const int km = k & 3;
+          const unsigned long long ow =
+              shfl64(km == 0 ? o[0] : km == 1 ? o[1] : km == 2 ? o[2] : o[3],
+                     8 * j + 1 + (k >> 2));
+          const float u = __ull2float_rn(ow >> 40) * 0x1p-24f;
+          const bool go = active && u < p;
+          if (!__any_sync(kFull, go)) break;
+          if (go) P *= p;
+          const float wgt = go ? (float)nR / ((float)nT * P) * inv_s : 0.f;
+          float4 fnext = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (leaf) {
+            // a leaf at the deepest level may hold any number of particles
+            const long long j0 = rT.link < 0 ? 0 : rT.link;
+            long long j1 = j0 + (rT.count < 0 ? 0 : rT.count);
+            if (j1 > a.n) j1 = a.n;
+            for (long long jj = j0; jj < j1; ++jj) {
+              const float4 pj = a.spm[jj];
+              if (kSelf && jj == qi) continue;
+              axpy(acc, wgt, mono(q, pj.x, pj.y, pj.z, pj.w, a.eps2));
+              nterm += go;
+            }
+          } else {
+            const int nc = rT.count < 8 ? rT.count : 8;
+            const long long cend = (long long)rT.link + nc < a.nodes ? rT.link + nc : a.nodes;
+            for (int c = rT.link; c < cend; ++c) {
+              const float4 cc = a.rec[c].com;
+              const float4 tc = mono(q, cc.x, cc.y, cc.z, cc.w, a.eps2);
+              axpy(acc, wgt, tc);
+              if (c == cidx) fnext = tc;
+            }
+            nterm += go ? (unsigned)nc : 0u;
+          }
+          axpy(acc, -wgt, fpar);
+          nterm += go;
+          active = go;
+          if (leaf) break;
+          rT = a.rec[cidx];
+          const int4 tc = a.topo[cidx];
+          nT = (long long)tc.y - tc.x;
+          fpar = fnext;
+        }
+      }
+    }
+    if (valid) {
+      float4 res;
+      res.x = a.G * acc.x; res.y = a.G * acc.y; res.z = a.G * acc.z; res.w = a.G * acc.w;
+      const unsigned dst = a.tperm[qi];
+      if (dst < a.m) a.out[dst] = res;
+      useful += nterm;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) useful += __shfl_xor_sync(kFull, useful, o);
+  if (lane == 0) {
+    if (useful) atomicAdd(&ctrl->step.executed, useful);
+    if (groups) atomicAdd(&ctrl->step.groups, groups);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
+                       DevCtrl *ctrl, cudaStream_t s) {
+  if (a.m <= 0) return cudaSuccess;
+  strata_kernel<<<1, 1024, 0, s>>>(a.rec, a.nodes, a.strata_level, strata_cap, strata, ctrl);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  static int per_sm[2] = {0, 0};
+  const int k = a.self_mode ? 1 : 0;
+  if (per_sm[k] == 0) {
+    if (a.self_mode)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[k], sbh_kernel<true>, kSbhThreads, 0);
+    else
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[k], sbh_kernel<false>, kSbhThreads, 0);
+    if (per_sm[k] < 1) per_sm[k] = 1;
+  }
+  const long long ngroups = (a.m + 31) / 32;
+  long long blocks = (long long)a.num_sms * per_sm[k];
+  const long long need = (ngroups + kSbhThreads / 32 - 1) / (kSbhThreads / 32);
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  if (a.self_mode)
+    sbh_kernel<true><<<(unsigned)blocks, kSbhThreads, 0, s>>>(a, ctrl);
+  else
+    sbh_kernel<false><<<(unsigned)blocks, kSbhThreads, 0, s>>>(a, ctrl);
+  return cudaGetLastError();
+}
+
+}  // namespace bh

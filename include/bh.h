@@ -64,6 +64,14 @@ typedef struct bh_ctx bh_ctx;
                                    one exactly (pointers, sizes, parameters,
                                    options) is captured once as a CUDA graph
                                    and replayed; 0: always launch kernels   */
+#define BH_OPT_ESTIMATOR     7  /* BH_EST_* (default BH_EST_BARNES_HUT)       */
+#define BH_OPT_SEED          8  /* stochastic estimator: 64-bit seed (default 0) */
+#define BH_OPT_SAMPLES       9  /* stochastic estimator: paths per stratum,
+                                   1..1024 (default 1)                       */
+#define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
+                                   strata, 0..6 (default 2: up to 64 strata,
+                                   the child count of the root of a tree with
+                                   4 children per axis)                      */
 
 #define BH_OPEN_VOTE  0  /* a cell is accepted for a group of targets only if
                             the opening test holds for every target of the
@@ -71,6 +79,34 @@ typedef struct bh_ctx bh_ctx;
 #define BH_OPEN_BOX   1  /* accepted if the test holds at the distance from
                             the centre of mass to the group's bounding box
                             (implies the vote; cheaper to evaluate)          */
+
+/*
+ * Estimators of the traversal stage.  Both use the same tree.
+ *
+ * BH_EST_BARNES_HUT: the deterministic walk with the opening test and warp
+ *   vote of the GASPHiA page (section "性能瓶颈分析").
+ * BH_EST_STOCHASTIC: stochastic Barnes-Hut (page "Stochastic Barnes-Hut
+ *   Approximation for Fast Summation on the GPU", section 方法, key designs
+ *   1-4), an unbiased Monte Carlo estimate of the direct sum:
+ *     F(q) = sum_R [ m_R f(p_R, q)
+ *                    + (1/S) sum_samples sum_{surviving steps T}
+ *                      Delta_T(q) (n_R / n_T) / P(reach T) ],
+ *     Delta_T(q) = sum_{c child of T} m_c f(p_c, q) - m_T f(p_T, q),
+ *   R over the strata (octree cells at level s and leaves above it), the
+ *   path from R towards particle I (uniform among R's particles), each step
+ *   surviving with probability min(1, max(1, b_T) / b_c), b = distance from
+ *   the query to the centre of mass (to the particle, for a leaf's child)
+ *   over the cell edge (half the leaf edge for a particle).  A leaf's children
+ *   are its particles; in self mode the query's own particle contributes 0.
+ *   Random numbers: Philox4x64-10 (Salmon et al., SC 2011), key (seed, 0),
+ *   counter (group, stratum, sample, block): block 0 word 0 gives
+ *   I = floor(word * n_R / 2^64), roulette step k uses block 1 + k/4 word
+ *   k%4 as u = (word >> 40) * 2^-24, and the step survives iff u < p.  A
+ *   group is 32 consecutive queries in Morton order; its queries share every
+ *   random number.  theta and BH_OPT_OPENING/GROUP do not apply.
+ */
+#define BH_EST_BARNES_HUT  0
+#define BH_EST_STOCHASTIC  1
 
 /* ---- debug knobs for bh_set_debug (tests only) ---- */
 #define BH_DBG_SPIN_LIMIT  1    /* polls before a device wait gives up
@@ -229,7 +265,9 @@ int bh_get_stage_times(bh_ctx *c, float *ms, int n);
 
 /*
  * Interaction counts of the last bh_compute (synchronises the device):
- * `executed` = source terms evaluated for valid targets by the group walk;
+ * `executed` = source terms evaluated for valid targets by the group walk
+ * (stochastic estimator: monopole evaluations, i.e. one per stratum plus,
+ * per surviving step, the cell's children (or particles) and the cell);
  * `groups` = number of target groups walked.
  */
 int bh_get_counters(bh_ctx *c, unsigned long long *executed,

@@ -79,7 +79,7 @@ def lib():
         L.orc_sbh.argtypes = [_f32p, C.c_int64, _i32p, _i64p, _i64p, _i64p, _i32p,
                               _f64p, C.c_float, C.c_double, C.c_double, _f32p, _vp,
                               _i64p, C.c_int64, C.c_uint64, C.c_int, C.c_int, _f64p,
-                              _i64p, _f64p, _f64p]
+                              _i64p, _f64p]
         L.orc_leapfrog.argtypes = [_f64p, _f64p, C.c_int64, C.c_double, C.c_double,
                                    C.c_double, C.c_int64]
         L.orc_num_threads.restype = C.c_int
@@ -296,7 +296,10 @@ class OracleBH:
         """Stochastic Barnes-Hut estimate for target rows ``rows`` (original
         indices, default all), in that order.  Queries share random numbers
         within a group of ``group`` consecutive Morton-ordered targets.
-        Returns (out[k,4], terms[k], absacc[k], abspot[k])."""
+        Returns (out[k,4], terms[k], scale[k,4]); scale columns: G * sum
+        |weighted term| of the acceleration and of the potential, and G * the
+        sums over cell terms of |weight| m / s^3 and |weight| m r / s^3
+        (s^2 = r^2 + eps^2), the sensitivities to centre-of-mass rounding."""
         order = self.target_order(tgt)
         k_all = order.shape[0]
         gpos = np.empty(k_all, np.int64)
@@ -312,14 +315,13 @@ class OracleBH:
         grp = np.ascontiguousarray(gpos[rr])
         out = np.zeros((k, 4), np.float64)
         terms = np.zeros(k, np.int64)
-        aa = np.zeros(k, np.float64)
-        ap = np.zeros(k, np.float64)
+        scale = np.zeros((k, 4), np.float64)
         t = self.tree
         lib().orc_sbh(self.spm, self.nnodes, t["level"], t["first"], t["count"],
                       t["child"], t["nchild"], self.com, float(self.cube[3]), self.G,
                       self.eps, pos, _ptr(selfj), grp, k, int(seed) & (2**64 - 1),
-                      int(strata_level), int(samples), out, terms, aa, ap)
-        return out, terms, aa, ap
+                      int(strata_level), int(samples), out, terms, scale)
+        return out, terms, scale
 
 
 def philox4x64(counter, key) -> np.ndarray:

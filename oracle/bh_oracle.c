@@ -572,8 +572,12 @@ void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4
 /*    share every random number, as the page shares seeds across a warp;     */
 /*  - S samples per stratum are averaged.                                    */
 /* grp[r]: group of target row r.  out: k rows (ax,ay,az,phi)*G.  terms:     */
-/* kernel evaluations per row.  absacc / abspot (may be NULL): G * sum of    */
-/* |weight * term| of the acceleration / potential, the rounding scale.      */
+/* kernel evaluations per row.  scale (may be NULL): k rows of four error    */
+/* scales, each times |G|: sum |weight * term| of the acceleration and of the */
+/* potential (the scale of summation rounding), and sum over cell terms of   */
+/* |weight| m / (r^2+eps^2)^{3/2} and |weight| m r / (r^2+eps^2)^{3/2}, the   */
+/* sensitivity of the acceleration and of the potential to a displacement of */
+/* the cells' centres of mass (which an fp32 implementation rounds).         */
 /* ------------------------------------------------------------------------ */
 static float beta32(const float *q, const float *p, float w)
 {
@@ -590,15 +594,25 @@ static float continue_prob(float beta_t, float beta_c)
     return p < 1.0f ? p : 1.0f;
 }
 
-/* one weighted softened term of mass m at s on target x */
+/* one weighted softened term of mass m at s on target x; sc accumulates the */
+/* four error scales (the last two only for cells, cell != 0)                */
 static int64_t wterm(const double *x, double sx, double sy, double sz, double m,
-                     double wgt, double eps2, double *acc, double *aa, double *ap)
+                     double wgt, double eps2, int cell, double *acc, double *sc)
 {
     double t[4] = {0, 0, 0, 0};
     pair_term(x, sx, sy, sz, m, eps2, t);
     for (int a = 0; a < 4; ++a) acc[a] += wgt * t[a];
-    *aa += fabs(wgt) * pair_mag(x, sx, sy, sz, m, eps2);
-    *ap += fabs(wgt * t[3]);
+    sc[0] += fabs(wgt) * pair_mag(x, sx, sy, sz, m, eps2);
+    sc[1] += fabs(wgt * t[3]);
+    if (cell) {
+        double dx = sx - x[0], dy = sy - x[1], dz = sz - x[2];
+        double r2 = dx * dx + dy * dy + dz * dz;
+        double s2 = r2 + eps2;
+        if (s2 > 0.0) {
+            sc[2] += fabs(wgt * m) / (s2 * sqrt(s2));
+            sc[3] += fabs(wgt * m) * sqrt(r2) / (s2 * sqrt(s2));
+        }
+    }
     return 1;
 }
 
@@ -607,8 +621,7 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
              const int32_t *nchild, const double *com, float L, double G,
              double eps, const float *tgt_pos, const int64_t *self_j,
              const int64_t *grp, int64_t k, uint64_t seed, int strata_level,
-             int samples, double *out, int64_t *terms, double *absacc,
-             double *abspot)
+             int samples, double *out, int64_t *terms, double *scale)
 {
     double eps2 = eps * eps;
     /* strata, in node order */
@@ -623,13 +636,13 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
         const float qf[3] = {tgt_pos[4 * r], tgt_pos[4 * r + 1], tgt_pos[4 * r + 2]};
         const double x[3] = {qf[0], qf[1], qf[2]};
         const int64_t self = self_j ? self_j[r] : -1;
-        double acc[4] = {0, 0, 0, 0}, aa = 0.0, ap = 0.0;
+        double acc[4] = {0, 0, 0, 0}, sc[4] = {0, 0, 0, 0};
         int64_t nterm = 0;
         for (int64_t si = 0; si < ns; ++si) {
             const int64_t R = strata[si];
             const double *cR = com + 4 * R;
             /* the stratum's monopole */
-            nterm += wterm(x, cR[0], cR[1], cR[2], cR[3], 1.0, eps2, acc, &aa, &ap);
+            nterm += wterm(x, cR[0], cR[1], cR[2], cR[3], 1.0, eps2, 1, acc, sc);
             for (int s = 0; s < samples; ++s) {
                 uint64_t ctr[4] = {(uint64_t)grp[r], (uint64_t)si, (uint64_t)s, 0};
                 uint64_t o[4], ou[4];
@@ -671,18 +684,18 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
                             if (j == self) continue;
                             const float *pj = spm + 4 * j;
                             nterm += wterm(x, pj[0], pj[1], pj[2], pj[3], wgt, eps2,
-                                           acc, &aa, &ap);
+                                           0, acc, sc);
                         }
                     } else {
                         for (int q = 0; q < nchild[T]; ++q) {
                             const double *cc = com + 4 * (child[T] + q);
                             nterm += wterm(x, cc[0], cc[1], cc[2], cc[3], wgt, eps2,
-                                           acc, &aa, &ap);
+                                           1, acc, sc);
                         }
                     }
                     const double *cT = com + 4 * T;
-                    nterm += wterm(x, cT[0], cT[1], cT[2], cT[3], -wgt, eps2, acc,
-                                   &aa, &ap);
+                    nterm += wterm(x, cT[0], cT[1], cT[2], cT[3], -wgt, eps2, 1,
+                                   acc, sc);
                     if (leaf) break;
                     T = c;
                 }
@@ -690,8 +703,8 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
         }
         for (int a = 0; a < 4; ++a) out[4 * r + a] = G * acc[a];
         if (terms) terms[r] = nterm;
-        if (absacc) absacc[r] = fabs(G) * aa;
-        if (abspot) abspot[r] = fabs(G) * ap;
+        if (scale)
+            for (int a = 0; a < 4; ++a) scale[4 * r + a] = fabs(G) * sc[a];
     }
     free(strata);
 }

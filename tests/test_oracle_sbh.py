@@ -91,7 +91,7 @@ def test_roulette_geometric_on_single_child_chain():
     split = min(lvl[c] for c in range(o.nnodes) if t["nchild"][c] > 1 and t["count"][c] == 20)
     assert split >= 12
     S = 4000
-    out, terms, _, _ = o.sbh(q, seed=5, strata_level=1, samples=S)
+    out, terms, _ = o.sbh(q, seed=5, strata_level=1, samples=S)
     # 2 strata monopoles; the lone far particle's leaf is near the query
     # (ratios below 1 for the leaf and its particle), so its one step always
     # survives: 2 terms per sample; then 2 terms (child, parent) per
@@ -118,9 +118,11 @@ def test_terms_and_scales_are_consistent():
     src = W.uniform_cube(500, 4)
     tgt = W.uniform_cube(40, 5)
     o = O.OracleBH(src, leaf_cap=16)
-    out, terms, aa, ap = o.sbh(tgt, seed=9)
+    out, terms, sc = o.sbh(tgt, seed=9)
+    aa, ap = sc[:, 0], sc[:, 1]
     ns = sum(1 for c in range(o.nnodes)
              if o.tree["level"][c] == 2 or (o.tree["level"][c] < 2 and o.tree["child"][c] < 0))
     assert (terms >= ns).all()
     assert (aa >= np.linalg.norm(out[:, :3], axis=1) * (1 - 1e-12)).all()
     assert (ap >= np.abs(out[:, 3]) * (1 - 1e-12)).all()
+    assert (sc[:, 2] > 0).all() and (sc[:, 3] > 0).all()
