@@ -61,12 +61,6 @@ __device__ __forceinline__ void philox4x64_10(unsigned long long c0,
   o[0] = c0; o[1] = c1; o[2] = c2; o[3] = c3;
 }
 
-__device__ __forceinline__ unsigned long long shfl64(unsigned long long v, int src) {
-  unsigned lo = __shfl_sync(kFull, (unsigned)v, src);
-  unsigned hi = __shfl_sync(kFull, (unsigned)(v >> 32), src);
-  return ((unsigned long long)hi << 32) | lo;
-}
-
 // beta = |q - p| / w, each operation rounded to fp32 in this order.
 __device__ __forceinline__ float beta_rn(const float4 &q, float px, float py,
                                          float pz, float w) {
@@ -149,8 +143,23 @@ __global__ void __launch_bounds__(1024) strata_kernel(const NodeRec *__restrict_
   if (threadIdx.x == 0) ctrl->step.strata = base_s < cap ? base_s : cap;
 }
 
+// Per-warp staging in shared memory: the Philox blocks of a batch of four
+// (stratum, sample) pairs (lane 8j + b holds block b of pair j), the four
+// strata, and eight child slots per pair (the stratum's children, then the
+// children of the current cell on its path).  Reads are warp-uniform
+// broadcasts.
+struct SbhWarp {
+  unsigned long long rng[32][4];
+  NodeRec strat[4];
+  int2 srange[4];            // (first, end) particles of each stratum
+  NodeRec child[32];
+  int2 crange[32];           // (first, end) particles of each child
+};
+
 template <bool kSelf>
 __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ctrl) {
+  __shared__ SbhWarp smem[kSbhThreads / 32];
+  SbhWarp &W = smem[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const float L = ctrl->keep.cube[0].w;
   const long long ns = ctrl->step.strata;
@@ -171,62 +180,85 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     unsigned nterm = 0;
     for (long long t0 = 0; t0 < npairs; t0 += 4) {
-      // lane 8j + b: block b of pair t0 + j
-      unsigned long long o[4];
       {
-        const long long t = t0 + (lane >> 3);
-        const long long r = t / S, smp = t - r * S;
-        philox4x64_10((unsigned long long)g, (unsigned long long)r,
-                      (unsigned long long)smp, (unsigned long long)(lane & 7),
+        // lane 8j + b: Philox block b of pair t0 + j, and child b of that
+        // pair's stratum (so the first step of all four paths is loaded)
+        const long long tl = t0 + (lane >> 3);
+        const int b = lane & 7;
+        const bool pair_ok = tl < npairs;
+        const long long rl = pair_ok ? tl / S : 0;
+        unsigned long long o[4];
+        philox4x64_10((unsigned long long)g, (unsigned long long)rl,
+                      (unsigned long long)(tl - rl * S), (unsigned long long)b,
                       a.seed, 0ull, o);
+        W.rng[lane][0] = o[0]; W.rng[lane][1] = o[1];
+        W.rng[lane][2] = o[2]; W.rng[lane][3] = o[3];
+        const int Rl = a.strata[rl];
+        const NodeRec srec = a.rec[Rl];
+        const int4 stop = a.topo[Rl];
+        if (b == 0) {
+          W.strat[lane >> 3] = srec;
+          W.srange[lane >> 3] = make_int2(stop.x, stop.y);
+        }
+        const int snc = (srec.flags & 1) ? 0 : (srec.count < 8 ? srec.count : 8);
+        if (pair_ok && b < snc && srec.link >= 0 && (long long)srec.link + b < a.nodes) {
+          W.child[lane] = a.rec[srec.link + b];
+          const int4 ct = a.topo[srec.link + b];
+          W.crange[lane] = make_int2(ct.x, ct.y);
+        }
+        __syncwarp();
       }
       const int jn = npairs - t0 < 4 ? (int)(npairs - t0) : 4;
       for (int j = 0; j < jn; ++j) {
-        const long long t = t0 + j;
-        const long long r = t / S, smp = t - r * S;
-        const int R = a.strata[r];
-        const NodeRec recR = a.rec[R];
-        const int4 topR = a.topo[R];
-        const long long nR = (long long)topR.y - topR.x;
+        const long long smp = (t0 + j) % S;
+        const int cb = 8 * j;
+        const NodeRec recR = W.strat[j];
+        const int2 rngR = W.srange[j];
+        const long long nR = (long long)rngR.y - rngR.x;
         float4 fpar = mono(q, recR.com.x, recR.com.y, recR.com.z, recR.com.w, a.eps2);
         if (smp == 0) {                      // the stratum's monopole, once
           axpy(acc, 1.f, fpar);
           nterm += 1;
         }
-        const unsigned long long w0 = shfl64(o[0], 8 * j);
-        long long J = topR.x + (long long)__umul64hi(w0, (unsigned long long)nR);
+        long long J = rngR.x + (long long)__umul64hi(W.rng[cb][0], (unsigned long long)nR);
         if (J < 0 || J >= a.n) J = 0;         // only a corrupt tree gets here
-        NodeRec rT = recR;
+        // the current cell T, warp-uniform
+        float4 tcom = recR.com;
+        int tlink = recR.link, tcount = recR.count, tflags = recR.flags;
         long long nT = nR;
         float P = 1.f;
         bool active = valid;
         for (int k = 0; k < kMaxSteps; ++k) {
-          const bool leaf = rT.flags & 1;
-          const int lv = (rT.flags >> 8) & 255;
+          const bool leaf = tflags & 1;
+          const int lv = (tflags >> 8) & 255;
           const float wT = edge(L, lv), wc = edge(L, lv + 1);
+          const int nc = leaf ? 0 : (tcount < 8 ? tcount : 8);
+          int ci = 0;
           float cx, cy, cz;
-          int cidx = -1;
           if (leaf) {
             const float4 pj = a.spm[J];
             cx = pj.x; cy = pj.y; cz = pj.z;
           } else {
+            const bool ok = tlink >= 0 && (long long)tlink + nc <= a.nodes;
+            if (k > 0) {                      // T's children into the slots
+              if (lane < nc && ok) {
+                W.child[cb + lane] = a.rec[tlink + lane];
+                const int4 ct = a.topo[tlink + lane];
+                W.crange[cb + lane] = make_int2(ct.x, ct.y);
+              }
+              __syncwarp();
+            }
             // the path child: the last child whose first particle is <= J
-            const int nc = rT.count < 8 ? rT.count : 8;
-            const bool in = lane < nc && rT.link >= 0 && rT.link + lane < a.nodes;
-            const int f = in ? a.topo[rT.link + lane].x : INT_MAX;
-            const unsigned bal = __ballot_sync(kFull, (long long)f <= J);
+            const unsigned bal = __ballot_sync(
+                kFull, ok && lane < nc && (long long)W.crange[cb + lane].x <= J);
             if (bal == 0u) break;             // only a corrupt tree gets here
-            cidx = rT.link + 31 - __clz(bal);
-            const float4 cc = a.rec[cidx].com;
+            ci = 31 - __clz(bal);
+            const float4 cc = W.child[cb + ci].com;
             cx = cc.x; cy = cc.y; cz = cc.z;
           }
-          const float p = continue_prob(beta_rn(q, rT.com.x, rT.com.y, rT.com.z, wT),
+          const float p = continue_prob(beta_rn(q, tcom.x, tcom.y, tcom.z, wT),
                                         beta_rn(q, cx, cy, cz, wc));
-          const int km = k & 3;
-          const unsigned long long ow =
-              shfl64(km == 0 ? o[0] : km == 1 ? o[1] : km == 2 ? o[2] : o[3],
-                     8 * j + 1 + (k >> 2));
-          const float u = __ull2float_rn(ow >> 40) * 0x1p-24f;
+          const float u = __ull2float_rn(W.rng[cb + 1 + (k >> 2)][k & 3] >> 40) * 0x1p-24f;
           const bool go = active && u < p;
           if (!__any_sync(kFull, go)) break;
           if (go) P *= p;
@@ -234,8 +266,8 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
           float4 fnext = make_float4(0.f, 0.f, 0.f, 0.f);
           if (leaf) {
             // a leaf at the deepest level may hold any number of particles
-            const long long j0 = rT.link < 0 ? 0 : rT.link;
-            long long j1 = j0 + (rT.count < 0 ? 0 : rT.count);
+            const long long j0 = tlink < 0 ? 0 : tlink;
+            long long j1 = j0 + (tcount < 0 ? 0 : tcount);
             if (j1 > a.n) j1 = a.n;
             for (long long jj = j0; jj < j1; ++jj) {
               const float4 pj = a.spm[jj];
@@ -244,13 +276,11 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
               nterm += go;
             }
           } else {
-            const int nc = rT.count < 8 ? rT.count : 8;
-            const long long cend = (long long)rT.link + nc < a.nodes ? rT.link + nc : a.nodes;
-            for (int c = rT.link; c < cend; ++c) {
-              const float4 cc = a.rec[c].com;
+            for (int c = 0; c < nc; ++c) {
+              const float4 cc = W.child[cb + c].com;
               const float4 tc = mono(q, cc.x, cc.y, cc.z, cc.w, a.eps2);
               axpy(acc, wgt, tc);
-              if (c == cidx) fnext = tc;
+              if (c == ci) fnext = tc;
             }
             nterm += go ? (unsigned)nc : 0u;
           }
@@ -258,12 +288,18 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
           nterm += go;
           active = go;
           if (leaf) break;
-          rT = a.rec[cidx];
-          const int4 tc = a.topo[cidx];
-          nT = (long long)tc.y - tc.x;
+          const NodeRec nx = W.child[cb + ci];
+          const int2 nr = W.crange[cb + ci];
+          tcom = nx.com;
+          tlink = nx.link;
+          tcount = nx.count;
+          tflags = nx.flags;
+          nT = (long long)nr.y - nr.x;
           fpar = fnext;
+          __syncwarp();                       // slots read before reuse
         }
       }
+      __syncwarp();                           // batch data read before reuse
     }
     if (valid) {
       float4 res;

@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="lattice1m_shuffled")
+    ap.add_argument("--workload", default=None,
+                    help="default lattice1m_shuffled (surface2e20 with --stochastic)")
     ap.add_argument("--theta", type=float, default=None,
                     help="override the workload's opening angle")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -67,6 +68,12 @@ def parse():
     ap.add_argument("--integrate", action="store_true",
                     help="time leapfrog simulation steps (bh_leapfrog) instead")
     ap.add_argument("--dt", type=float, default=1e-4)
+    ap.add_argument("--stochastic", action="store_true",
+                    help="time the stochastic Barnes-Hut estimator (default workload "
+                         "surface2e20) beside the deterministic walk")
+    ap.add_argument("--samples", type=int, default=1)
+    ap.add_argument("--strata-level", type=int, default=2)
+    ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
 
@@ -491,8 +498,97 @@ def run_integrate(args, rank, local_rank, world):
     return 0
 
 
+def run_stochastic(args, rank, local_rank, world):
+    """Stochastic Barnes-Hut steps (page "Stochastic Barnes-Hut Approximation
+    for Fast Summation on the GPU") timed beside the deterministic walk on the
+    same workload, with the potential's absolute error against the direct sum
+    on sampled targets (the page's table reports mean / median / max absolute
+    error of the potential and the time)."""
+    import numpy as np
+    import torch
+
+    import barnes_hut_body_gb300 as B
+    import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    src, tgt, G, eps, theta = W.make(args.workload)
+    theta = args.theta if args.theta is not None else theta
+    n = src.shape[0]
+    m = n if tgt is None else tgt.shape[0]
+    d_src = torch.from_numpy(src).to(device)
+    d_tgt = None if tgt is None else torch.from_numpy(tgt).to(device)
+    d_out = torch.empty((m, 4), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    rows = W.error_sample(m, 4096, seed=7)
+    d_rows = torch.from_numpy(rows).to(device)
+    ref = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank)
+    exact = ref.direct(d_src, d_src[d_rows] if d_tgt is None else d_tgt[d_rows])
+    exact = exact.cpu().numpy().astype(np.float64)
+    ref.close()
+    stream = torch.cuda.current_stream(device)
+
+    def timed(bh):
+        for _ in range(max(args.warmup, 3)):
+            bh.compute(d_src, d_tgt, d_out)
+        if bh.status() != 0:
+            raise RuntimeError(B.bh_last_error(bh.ctx))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world, device)
+        torch.cuda.synchronize(device)
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            bh.compute(d_src, d_tgt, d_out)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(device)
+        ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
+        executed, _ = B.bh_get_counters(bh.ctx)
+        got = d_out.index_select(0, d_rows).cpu().numpy().astype(np.float64)
+        e = np.abs(got[:, 3] - exact[:, 3])
+        return ms, executed, dict(mean=float(e.mean()), median=float(np.median(e)),
+                                  max=float(e.max()))
+
+    sto = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank,
+                      estimator=B.BH_EST_STOCHASTIC, samples=args.samples,
+                      strata_level=args.strata_level, seed=args.seed)
+    ms_s, ex_s, err_s = timed(sto)
+    sto.close()
+    det = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank)
+    ms_d, ex_d, err_d = timed(det)
+    det.close()
+    props = torch.cuda.get_device_properties(device)
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "stochastic_queries_per_s",
+            "value": sum_over_ranks(m, world, device) / (ms_s / 1e3), "unit": "queries/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_s, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(args.workload, src, tgt, theta, eps),
+                           estimator="stochastic", samples=args.samples,
+                           strata_level=args.strata_level, seed=args.seed,
+                           l2="flushed (256 MiB write) before every step"),
+            "evaluations_per_query": ex_s / m,
+            "pot_abs_error": err_s,
+            "roofline": {"bound": "alu", "achieved": ex_s * FLOPS_PER_TERM / (ms_s / 1e3) / 1e12,
+                         "peak": peak, "unit": "TFLOP/s",
+                         "frac": ex_s * FLOPS_PER_TERM / (ms_s / 1e3) / 1e12 / peak,
+                         "traffic": None, "note": "whole step, evaluations x 20 flop"},
+            "deterministic": {"theta": theta, "ms_per_step": ms_d,
+                              "evaluations_per_query": ex_d / m, "pot_abs_error": err_d},
+            "error_sample": "4096 targets (PCG64 seed 7) against the direct-sum kernel",
+            "gpu_launches": None}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.workload is None:
+        args.workload = "surface2e20" if args.stochastic else "lattice1m_shuffled"
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
@@ -500,6 +596,8 @@ def main():
         return run_direct(args, rank, local_rank, world)
     if args.integrate:
         return run_integrate(args, rank, local_rank, world)
+    if args.stochastic:
+        return run_stochastic(args, rank, local_rank, world)
     return run_ours(args, rank, local_rank, world)
 
 
