@@ -18,9 +18,9 @@
 // stops.  Random numbers: Philox4x64-10 with key (seed, 0) and counter
 // (group, stratum, sample, block); block 0 word 0 gives I, roulette step k
 // reads block 1 + k/4, word k%4.  The 32 lanes compute the 8 blocks of 4
-// (stratum, sample) pairs at once.  The roulette decision u < p is taken in
-// fp32 with every operation rounded as written (no contraction), so it
-// depends only on the inputs and the tree.
+// (stratum, sample) pairs at once.  The roulette decision is taken in fp32
+// on squared distances with every operation rounded as written (no
+// contraction), so it depends only on the inputs and the tree.
 #include <climits>
 
 #include "bh_internal.h"
@@ -61,19 +61,28 @@ __device__ __forceinline__ void philox4x64_10(unsigned long long c0,
   o[0] = c0; o[1] = c1; o[2] = c2; o[3] = c3;
 }
 
-// beta = |q - p| / w, each operation rounded to fp32 in this order.
-__device__ __forceinline__ float beta_rn(const float4 &q, float px, float py,
-                                         float pz, float w) {
+// |q - p|^2, each operation rounded to fp32 in this order.
+__device__ __forceinline__ float dist2_rn(const float4 &q, float px, float py, float pz) {
   const float dx = __fsub_rn(q.x, px), dy = __fsub_rn(q.y, py),
               dz = __fsub_rn(q.z, pz);
-  float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
-  d2 = __fadd_rn(d2, __fmul_rn(dz, dz));
-  return __fdiv_rn(__fsqrt_rn(d2), w);
+  const float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
+  return __fadd_rn(d2, __fmul_rn(dz, dz));
 }
 
-__device__ __forceinline__ float continue_prob(float bt, float bc) {
-  if (!(bc > 0.f)) return 1.f;
-  const float p = __fdiv_rn(fmaxf(1.f, bt), bc);
+// The roulette.  The continue probability min(1, max(1, beta_T) / beta_c),
+// beta = r / w, with the child's edge w_T / 2, is min(1, max(w_T, r_T) /
+// (2 r_c)); the draw u survives iff (4 (u u)) r_c^2 < max(w_T w_T, r_T^2),
+// every operation rounded to fp32 as written.
+__device__ __forceinline__ bool survives(float u, float wT, float dT2, float dc2) {
+  const float lhs = __fmul_rn(__fmul_rn(4.f, __fmul_rn(u, u)), dc2);
+  const float rhs = fmaxf(__fmul_rn(wT, wT), dT2);
+  return lhs < rhs;
+}
+
+// Its probability, for the path weight only.
+__device__ __forceinline__ float survival_prob(float wT, float dT2, float dc2) {
+  if (!(dc2 > 0.f)) return 1.f;
+  const float p = sqrtf(fmaxf(wT * wT, dT2) / (4.f * dc2));
   return p < 1.f ? p : 1.f;
 }
 
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
         for (int k = 0; k < kMaxSteps; ++k) {
           const bool leaf = tflags & 1;
           const int lv = (tflags >> 8) & 255;
-          const float wT = edge(L, lv), wc = edge(L, lv + 1);
+          const float wT = edge(L, lv);
           const int nc = leaf ? 0 : (tcount < 8 ? tcount : 8);
           int ci = 0;
           float cx, cy, cz;
@@ -256,13 +265,13 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
             const float4 cc = W.child[cb + ci].com;
             cx = cc.x; cy = cc.y; cz = cc.z;
           }
-          const float p = continue_prob(beta_rn(q, tcom.x, tcom.y, tcom.z, wT),
-                                        beta_rn(q, cx, cy, cz, wc));
+          const float dT2 = dist2_rn(q, tcom.x, tcom.y, tcom.z);
+          const float dc2 = dist2_rn(q, cx, cy, cz);
           const float u = __ull2float_rn(W.rng[cb + 1 + (k >> 2)][k & 3] >> 40) * 0x1p-24f;
-          const bool go = active && u < p;
+          const bool go = active && survives(u, wT, dT2, dc2);
           if (!__any_sync(kFull, go)) break;
-          if (go) P *= p;
-          const float wgt = go ? (float)nR / ((float)nT * P) * inv_s : 0.f;
+          if (go) P *= survival_prob(wT, dT2, dc2);
+          const float wgt = go ? __fdividef((float)nR * inv_s, (float)nT * P) : 0.f;
           float4 fnext = make_float4(0.f, 0.f, 0.f, 0.f);
           if (leaf) {
             // a leaf at the deepest level may hold any number of particles

@@ -101,9 +101,12 @@ typedef struct bh_ctx bh_ctx;
  *   Random numbers: Philox4x64-10 (Salmon et al., SC 2011), key (seed, 0),
  *   counter (group, stratum, sample, block): block 0 word 0 gives
  *   I = floor(word * n_R / 2^64), roulette step k uses block 1 + k/4 word
- *   k%4 as u = (word >> 40) * 2^-24, and the step survives iff u < p.  A
- *   group is 32 consecutive queries in Morton order; its queries share every
- *   random number.  theta and BH_OPT_OPENING/GROUP do not apply.
+ *   k%4 as u = (word >> 40) * 2^-24.  With the child's edge w_T / 2,
+ *   p = min(1, max(w_T, r_T) / (2 r_c)), and the step survives iff
+ *   (4 (u u)) r_c^2 < max(w_T w_T, r_T^2) in fp32, every operation rounded
+ *   as written.  A group is 32 consecutive queries in Morton order; its
+ *   queries share every random number.  theta and BH_OPT_OPENING/GROUP do
+ *   not apply.
  */
 #define BH_EST_BARNES_HUT  0
 #define BH_EST_STOCHASTIC  1

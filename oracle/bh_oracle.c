@@ -562,9 +562,12 @@ void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4
 /*    a particle's size is half the edge of its leaf;                       */
 /*  - far-field ratio beta(T) = |q - p_T| / w_T, p_T the centre of mass, w_T */
 /*    the cell edge; continue from T to the path child c with probability   */
-/*    p = min(1, max(1, beta(T)) / beta(c)), 1 where beta(c) = 0; the       */
-/*    decision u < p is taken in fp32 (the page computes in single          */
-/*    precision), everything else in fp64;                                  */
+/*    p = min(1, max(1, beta(T)) / beta(c)), 1 where beta(c) = 0.  The child */
+/*    edge is w_T / 2 (a cell's or a particle's), so p = min(1, max(w_T,     */
+/*    r_T) / (2 r_c)), r = distance to the centre of mass (the particle).    */
+/*    The decision u < p is taken in fp32 (the page computes in single       */
+/*    precision) on squares, with every operation rounded as written:       */
+/*    (4 (u u)) r_c^2 < max(w_T w_T, r_T^2); everything else in fp64;       */
 /*  - random numbers: Philox4x64-10, key (seed, 0), counter (group, stratum, */
 /*    sample, block).  Block 0 word 0 gives I = floor(o * n_R / 2^64);       */
 /*    roulette step k uses block 1 + k/4, word k%4, as u = (o >> 40) 2^-24.  */
@@ -579,19 +582,29 @@ void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4
 /* sensitivity of the acceleration and of the potential to a displacement of */
 /* the cells' centres of mass (which an fp32 implementation rounds).         */
 /* ------------------------------------------------------------------------ */
-static float beta32(const float *q, const float *p, float w)
+/* squared distance in fp32, rounded in this order */
+static float dist2_32(const float *q, const float *p)
 {
     float dx = q[0] - p[0], dy = q[1] - p[1], dz = q[2] - p[2];
     float d2 = dx * dx + dy * dy;
-    d2 = d2 + dz * dz;
-    return sqrtf(d2) / w;
+    return d2 + dz * dz;
 }
 
-static float continue_prob(float beta_t, float beta_c)
+/* the roulette: does the step from T to its path child survive draw u? */
+static int survives(float u, float wT, float dT2, float dc2)
 {
-    if (!(beta_c > 0.0f)) return 1.0f;
-    float p = fmaxf(1.0f, beta_t) / beta_c;
-    return p < 1.0f ? p : 1.0f;
+    float lhs = (4.0f * (u * u)) * dc2;
+    float rhs = fmaxf(wT * wT, dT2);
+    return lhs < rhs;
+}
+
+/* the survival probability of that step, for the weight (fp64) */
+static double survival_prob(float wT, float dT2, float dc2)
+{
+    if (!(dc2 > 0.0f)) return 1.0;
+    double rhs = fmax((double)wT * (double)wT, (double)dT2);
+    double p = sqrt(rhs / (4.0 * (double)dc2));
+    return p < 1.0 ? p : 1.0;
 }
 
 /* one weighted softened term of mass m at s on target x; sc accumulates the */
@@ -655,7 +668,6 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
                 for (int step = 0;; ++step) {
                     const int leaf = child[T] < 0;
                     const float wT = ldexpf(L, -level[T]);
-                    const float wc = ldexpf(L, -(level[T] + 1));
                     const float pT[3] = {(float)com[4 * T], (float)com[4 * T + 1],
                                          (float)com[4 * T + 2]};
                     int64_t c = -1;              /* path child node (internal T) */
@@ -669,14 +681,14 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
                         }
                         for (int a = 0; a < 3; ++a) pc[a] = (float)com[4 * c + a];
                     }
-                    float p = continue_prob(beta32(qf, pT, wT), beta32(qf, pc, wc));
+                    const float dT2 = dist2_32(qf, pT), dc2 = dist2_32(qf, pc);
                     if (step % 4 == 0) {
                         ctr[3] = (uint64_t)(1 + step / 4);
                         orc_philox4x64(ctr, key, ou);
                     }
                     float u = (float)(ou[step % 4] >> 40) * 0x1p-24f;
-                    if (!(u < p)) break;         /* roulette ends the path */
-                    P *= (double)p;
+                    if (!survives(u, wT, dT2, dc2)) break;   /* roulette ends the path */
+                    P *= survival_prob(wT, dT2, dc2);
                     double wgt = ((double)count[R] / (double)count[T]) / P / samples;
                     /* Delta_T: children's monopoles minus T's own */
                     if (leaf) {
