@@ -22,6 +22,9 @@ the web page section it restates (see the C file's header):
   Fast Summation on the GPU" page, section 方法: telescoping path sums, Russian
   roulette on the path length, stratification), with ``philox4x64`` as its
   counter-based random numbers.
+* ``neighbors`` -- SPH neighbour search written out as brute force ("树结构"
+  page, sections 粒子领域搜索 and 树遍历计算; GASPHiA's per-node maximum
+  smoothing length), the distance test in fp32.
 * ``leapfrog`` -- kick-drift-kick time stepping with brute-force forces (the
   pages show an N-body run advanced in time but print no integrator).
 """
@@ -80,6 +83,8 @@ def lib():
                               _f64p, C.c_float, C.c_double, C.c_double, _f32p, _vp,
                               _i64p, C.c_int64, C.c_uint64, C.c_int, C.c_int, _f64p,
                               _i64p, _f64p]
+        L.orc_neighbors.argtypes = [_f32p, _f32p, C.c_int64, C.c_float, C.c_int, _i64p,
+                                    C.c_int64, _i64p, _vp, _vp]
         L.orc_leapfrog.argtypes = [_f64p, _f64p, C.c_int64, C.c_double, C.c_double,
                                    C.c_double, C.c_int64]
         L.orc_num_threads.restype = C.c_int
@@ -322,6 +327,31 @@ class OracleBH:
                       self.eps, pos, _ptr(selfj), grp, k, int(seed) & (2**64 - 1),
                       int(strata_level), int(samples), out, terms, scale)
         return out, terms, scale
+
+
+NB_GATHER, NB_SYMMETRIC = 0, 1
+
+
+def neighbors(pm, h, kappa: float = 2.0, mode: int = NB_SYMMETRIC, rows=None,
+              with_lists: bool = True):
+    """Brute-force neighbour search.  Returns (counts[k], lists) for query
+    rows ``rows`` (default all); lists[r] holds row r's neighbour indices in
+    ascending order (None without ``with_lists``)."""
+    pm = _rows(pm)
+    h = np.ascontiguousarray(h, np.float32)
+    n = pm.shape[0]
+    rr = np.arange(n, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    k = rr.shape[0]
+    counts = np.zeros(k, np.int64)
+    lib().orc_neighbors(pm, h, n, float(kappa), int(mode), rr, k, counts, None, None)
+    if not with_lists:
+        return counts, None
+    offs = np.zeros(k + 1, np.int64)
+    np.cumsum(counts, out=offs[1:])
+    flat = np.zeros(max(int(offs[-1]), 1), np.int64)
+    lib().orc_neighbors(pm, h, n, float(kappa), int(mode), rr, k, counts,
+                        offs.ctypes.data_as(C.c_void_p), flat.ctypes.data_as(C.c_void_p))
+    return counts, [flat[offs[r]:offs[r + 1]] for r in range(k)]
 
 
 def philox4x64(counter, key) -> np.ndarray:

@@ -720,3 +720,50 @@ void orc_sbh(const float *spm, int64_t nnodes, const int32_t *level,
     }
     free(strata);
 }
+
+/* ------------------------------------------------------------------------ */
+/* SPH neighbour search ([S] "树结构（基于根据 Burtscher 和 Pingali 的研究）", */
+/* sections 1 粒子领域搜索 and 实现步骤 / 树遍历计算: find the particles within */
+/* the kernel scale of each query; [T] GASPHiA keeps a per-node maximum      */
+/* smoothing length, d_node_hmax, for that search).  The definition written */
+/* out: particle j != i is a neighbour of i iff                              */
+/*   |x_i - x_j|^2 < (kappa * H)^2,  H = max(h_i, h_j)  (mode 1, symmetric)  */
+/*                                   H = h_i            (mode 0, gather)    */
+/* Readings: kappa is the kernel's support in units of h; the test is taken  */
+/* in fp32 (the pages' particle data are single precision) with every       */
+/* operation rounded as written: d = x_i - x_j per axis,                    */
+/* r2 = (dx dx + dy dy) + dz dz, s = kappa H, s2 = s s, neighbour iff       */
+/* r2 < s2.  Brute force over all pairs, no tree.                           */
+/* rows: the k query rows (indices into pm); counts[r]: neighbours of row   */
+/* r; list (may be NULL): row r's neighbours in ascending index order at    */
+/* list[offs[r] ..], offs (k+1 entries) given by the caller.                */
+/* ------------------------------------------------------------------------ */
+static int is_neighbour(const float *pm, const float *h, int64_t i, int64_t j,
+                        float kappa, int mode)
+{
+    float dx = pm[4 * i] - pm[4 * j];
+    float dy = pm[4 * i + 1] - pm[4 * j + 1];
+    float dz = pm[4 * i + 2] - pm[4 * j + 2];
+    float r2 = dx * dx + dy * dy;
+    r2 = r2 + dz * dz;
+    float H = mode == 1 ? fmaxf(h[i], h[j]) : h[i];
+    float s = kappa * H;
+    float s2 = s * s;
+    return r2 < s2;
+}
+
+void orc_neighbors(const float *pm, const float *h, int64_t n, float kappa,
+                   int mode, const int64_t *rows, int64_t k, int64_t *counts,
+                   const int64_t *offs, int64_t *list)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < k; ++r) {
+        int64_t i = rows[r], c = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            if (j == i || !is_neighbour(pm, h, i, j, kappa, mode)) continue;
+            if (list) list[offs[r] + c] = j;
+            ++c;
+        }
+        counts[r] = c;
+    }
+}

@@ -28,8 +28,8 @@ import numpy as np
 
 __all__ = [
     "rng", "uniform_cube", "lattice", "ellipsoid_surfaces", "query_grid",
-    "galaxy_pair", "plummer", "uniform_ball", "error_sample", "WORKLOADS",
-    "make",
+    "galaxy_pair", "plummer", "uniform_ball", "sph_plummer", "uniform_sph",
+    "error_sample", "WORKLOADS", "make",
 ]
 
 
@@ -210,6 +210,32 @@ def uniform_ball(n: int = 1 << 16, seed: int = 6, radius: float = 1.0,
     g = rng(seed)
     r = radius * np.cbrt(g.random(n))
     return _pack(r[:, None] * _unit_vectors(g, n), total_mass / n)
+
+
+def sph_plummer(n: int = 1 << 20, seed: int = 4, a: float = 0.1,
+                trunc: float = 20.0, n_ngb: float = 64.0):
+    """Plummer sphere (as ``plummer``) with SPH smoothing lengths.
+
+    h_i = eta * (m / rho(r_i))^(1/3) from the analytic Plummer density
+    rho(r) = 3 M / (4 pi a^3) (1 + r^2/a^2)^(-5/2) (M = 1, m = 1/N), with
+    eta chosen so that a sphere of radius 2 h holds n_ngb particles on
+    average: (4/3) pi (2 h)^3 rho / m = n_ngb, i.e. eta^3 = 3 n_ngb / (32 pi).
+    Returns (pos_mass float32 (n, 4), h float32 (n,)).
+    """
+    pm = plummer(n, seed=seed, a=a, trunc=trunc)
+    r = np.linalg.norm(pm[:, :3].astype(np.float64), axis=1)
+    rho = 3.0 / (4.0 * np.pi * a ** 3) * (1.0 + (r / a) ** 2) ** -2.5
+    eta = (3.0 * n_ngb / (32.0 * np.pi)) ** (1.0 / 3.0)
+    h = eta * np.cbrt((1.0 / n) / rho)
+    return pm, h.astype(np.float32)
+
+
+def uniform_sph(n: int = 1 << 20, seed: int = 0, n_ngb: float = 64.0):
+    """Uniform cube [0,1)^3 with one smoothing length for all particles,
+    chosen as in ``sph_plummer``: (4/3) pi (2 h)^3 n = n_ngb."""
+    pm = uniform_cube(n, seed)
+    h = (3.0 * n_ngb / (32.0 * np.pi * n)) ** (1.0 / 3.0)
+    return pm, np.full(n, h, np.float32)
 
 
 def error_sample(n: int, s: int = 16384, seed: int = 5) -> np.ndarray:
