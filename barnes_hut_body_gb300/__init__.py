@@ -36,7 +36,7 @@ EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
             "bh_set_debug", "bh_compute", "bh_compute_host", "bh_direct",
             "bh_sync_status", "bh_get_stage_times", "bh_get_counters",
             "bh_debug_export", "bh_count_interactions", "bh_direct_static",
-            "bh_leapfrog", "bh_last_error")
+            "bh_leapfrog", "bh_neighbors", "bh_last_error")
 
 _lib = None
 
@@ -71,6 +71,7 @@ def lib():
         L.bh_count_interactions.argtypes = [vp, vp, C.POINTER(C.c_ulonglong), vp]
         L.bh_direct_static.argtypes = [vp, sz, vp, sz, f, f, vp, vp]
         L.bh_leapfrog.argtypes = [vp, vp, vp, sz, vp, f, i, i, vp]
+        L.bh_neighbors.argtypes = [vp, vp, vp, sz, f, i, vp, vp, vp, sz, vp]
         L.bh_last_error.argtypes = [vp]
         L.bh_last_error.restype = C.c_char_p
         for name in EXPORTED:
@@ -191,6 +192,38 @@ def bh_leapfrog(ctx, pos_mass, vel, acc_pot, dt: float, nsteps: int,
     flags = BH_LF_ACC_VALID if acc_valid else 0
     _check(ctx, lib().bh_leapfrog(ctx, p, v, n, a, float(dt), int(nsteps), flags,
                                   _stream(pos_mass, stream)))
+
+
+BH_NB_GATHER, BH_NB_SYMMETRIC = 0, 1
+
+
+def bh_neighbors(ctx, pos_mass, h, kappa: float = 2.0, mode: int = BH_NB_SYMMETRIC,
+                 lists: bool = True, stream=None):
+    """SPH neighbour search on device tensors: pos_mass (n, 4) and h (n,)
+    float32.  Returns (counts uint32 (n,), offsets uint64 (n+1,), list
+    uint32 (total,)) as CUDA tensors; with ``lists`` False only counts (the
+    other two None).  Sizing the list synchronises the stream once."""
+    import torch
+    p, n = _rows_ptr(pos_mass, "pos_mass")
+    if h.dtype != torch.float32 or not h.is_contiguous() or h.numel() != n or \
+            h.device != pos_mass.device:
+        raise ValueError("h must be a contiguous float32 tensor of n values on the same device")
+    dev = pos_mass.device
+    counts = torch.empty(n, dtype=torch.int32, device=dev)
+    st = _stream(pos_mass, stream)
+    if not lists:
+        _check(ctx, lib().bh_neighbors(ctx, p, h.data_ptr(), n, float(kappa), int(mode),
+                                       counts.data_ptr(), None, None, 0, st))
+        return counts, None, None
+    offsets = torch.empty(n + 1, dtype=torch.int64, device=dev)
+    _check(ctx, lib().bh_neighbors(ctx, p, h.data_ptr(), n, float(kappa), int(mode),
+                                   counts.data_ptr(), offsets.data_ptr(), None, 0, st))
+    total = int(offsets[n].item()) if n else 0
+    lst = torch.empty(max(total, 1), dtype=torch.int32, device=dev)
+    _check(ctx, lib().bh_neighbors(ctx, p, h.data_ptr(), n, float(kappa), int(mode),
+                                   counts.data_ptr(), offsets.data_ptr(), lst.data_ptr(),
+                                   total, st))
+    return counts, offsets, lst[:total]
 
 
 def _host_rows(a, name):

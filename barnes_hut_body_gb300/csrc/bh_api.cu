@@ -31,6 +31,11 @@ struct bh_ctx {
   unsigned long long seed = 0;
   int *strata = nullptr;
   int strata_cap = 0;
+  // neighbour search scratch
+  NbNode *nb_nodes = nullptr;
+  float *nb_h = nullptr;
+  unsigned long long *nb_scan = nullptr;
+  long long nb_cap_n = 0, nb_cap_nodes = 0;
   unsigned spin_limit = 1u << 22;
   std::string err;
 
@@ -338,6 +343,9 @@ int bh_destroy(bh_ctx *c) {
     free_targets(c);
     free_dev(c->status);
     free_dev(c->strata);
+    free_dev(c->nb_nodes);
+    free_dev(c->nb_h);
+    free_dev(c->nb_scan);
     free_dev(c->ctrl);
     free_dev(c->partials);
     free_dev(c->dpartial);
@@ -610,6 +618,71 @@ int bh_direct(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
                                 M, self, c->eps, c->G, c->dpartial, c->dpartial_cap,
                                 reinterpret_cast<float4 *>(acc_pot), c->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(c, e, "direct launch");
+  return BH_OK;
+}
+
+int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
+                 float kappa, int mode, unsigned int *counts,
+                 unsigned long long *offsets, unsigned int *list, size_t list_cap,
+                 void *stream) {
+  if (!c) return BH_EINVAL;
+  c->err.clear();
+  int rc;
+  if ((rc = check_rows(c, pos_mass, n, "pos_mass")) != BH_OK) return rc;
+  if (n && !h) return fail(c, BH_EINVAL, "h is NULL");
+  if (n && !counts) return fail(c, BH_EINVAL, "counts is NULL");
+  if (list && !offsets) return fail(c, BH_EINVAL, "a list needs offsets");
+  if (!(kappa > 0.f) || !isfinite(kappa)) return fail(c, BH_EINVAL, "kappa must be finite and > 0");
+  if (mode != BH_NB_GATHER && mode != BH_NB_SYMMETRIC) return fail(c, BH_EINVAL, "unknown neighbour mode");
+  if (n > 0xffffffffULL) return fail(c, BH_EINVAL, "too many particles for 32-bit indices");
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceGuard g(c->device);
+  c->last_valid = false;
+  const long long N = (long long)n;
+  if (N == 0) {
+    if (offsets) {
+      cudaError_t e = cudaMemsetAsync(offsets, 0, sizeof(unsigned long long), s);
+      if (e != cudaSuccess) return cuda_fail(c, e, "memset");
+    }
+    return BH_OK;
+  }
+  if ((rc = ensure_sources(c, N)) != BH_OK) return rc;
+  if (c->nb_cap_n < c->cap_n || c->nb_cap_nodes < c->cap_nodes) {
+    cudaDeviceSynchronize();
+    free_dev(c->nb_nodes); free_dev(c->nb_h); free_dev(c->nb_scan);
+    c->nb_cap_n = c->nb_cap_nodes = 0;
+    if (!alloc_dev(c->nb_nodes, c->cap_nodes) || !alloc_dev(c->nb_h, c->cap_n) ||
+        !alloc_dev(c->nb_scan, c->cap_n / 1024 + 2))
+      return fail(c, BH_ENOMEM, "neighbour search scratch");
+    c->nb_cap_n = c->cap_n;
+    c->nb_cap_nodes = c->cap_nodes;
+  }
+  const float4 *pm = reinterpret_cast<const float4 *>(pos_mass);
+  int fb = 0;
+  cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
+  if (e == cudaSuccess) e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
+  if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
+  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
+  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
+  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
+  NbArgs a;
+  a.spm = c->spm;
+  a.sh = c->nb_h;
+  a.n = N;
+  a.topo = c->build.topo;
+  a.nodes = c->nb_nodes;
+  a.nodes_cap = c->build.cap_nodes;
+  a.perm = c->sort.idx[fb];
+  a.kappa = kappa;
+  a.symmetric = mode == BH_NB_SYMMETRIC ? 1 : 0;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.list = list;
+  a.list_cap = list ? (unsigned long long)list_cap : 0ull;
+  a.num_sms = c->num_sms;
+  if (e == cudaSuccess)
+    e = launch_neighbors(a, h, c->build.parent, c->build.arrive, c->nb_scan, c->ctrl, s);
+  if (e != cudaSuccess) return cuda_fail(c, e, "neighbour search launch");
   return BH_OK;
 }
 

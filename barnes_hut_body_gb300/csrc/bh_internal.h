@@ -150,6 +150,32 @@ struct SbhArgs {
 };
 cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
                        DevCtrl *ctrl, cudaStream_t s);
+
+// Neighbour search: per node the particles' bounding box and largest
+// smoothing length, 32 bytes.
+struct alignas(16) NbNode {
+  float4 lo_h;               // (lo.x, lo.y, lo.z, max h)
+  float4 hi;                 // (hi.x, hi.y, hi.z, unused)
+};
+struct NbArgs {
+  const float4 *spm;         // sorted particles
+  float *sh;                 // sorted smoothing lengths (written)
+  long long n;
+  const int4 *topo;
+  NbNode *nodes;
+  long long nodes_cap;
+  const unsigned int *perm;  // sorted -> caller index
+  float kappa;
+  int symmetric;
+  unsigned int *counts;      // caller order
+  unsigned long long *offsets;   // caller order, n + 1, or null
+  unsigned int *list;        // or null
+  unsigned long long list_cap;
+  int num_sms;
+};
+cudaError_t launch_neighbors(const NbArgs &a, const float *h, const int *parent,
+                             int *arrive, unsigned long long *scan_tmp,
+                             DevCtrl *ctrl, cudaStream_t s);
 cudaError_t launch_count(const WalkArgs &a, unsigned int *counts, DevCtrl *ctrl,
                          cudaStream_t s);
 

@@ -260,6 +260,41 @@ int bh_leapfrog(bh_ctx *c, float *pos_mass, float *vel, size_t n,
 int bh_sync_status(bh_ctx *c, void *stream);
 
 /*
+ * SPH neighbour search on the same octree ("树结构（基于根据 Burtscher 和
+ * Pingali 的研究）" page, sections 粒子领域搜索 and 树遍历计算: the particles
+ * within the kernel scale of each query, found by walking the tree; GASPHiA
+ * keeps the per-node maximum smoothing length d_node_hmax for this search).
+ * Particle j != i is a neighbour of i iff
+ *     |x_i - x_j|^2 < (kappa H)^2,   H = max(h_i, h_j)  (BH_NB_SYMMETRIC)
+ *                                    H = h_i            (BH_NB_GATHER)
+ * with the test taken in fp32, every operation rounded as written:
+ * d = x_i - x_j per axis, r2 = (dx dx + dy dy) + dz dz, s = kappa H,
+ * neighbour iff r2 < s s.  The results are exact (no tolerance).
+ *
+ *   pos_mass  device, n rows (x,y,z,m); m is not used.
+ *   h         device, n floats, smoothing lengths, finite and >= 0
+ *             (otherwise the status word reads BH_EINVAL).
+ *   kappa     kernel support in units of h (2 for the cubic spline), > 0.
+ *   counts    device uint32[n], required: neighbours of particle i at i.
+ *   offsets   device uint64[n+1] or NULL: exclusive scan of counts
+ *             (offsets[n] = total).
+ *   list      device uint32[list_cap] or NULL (needs offsets): particle i's
+ *             neighbours (caller indices) at list[offsets[i] .. offsets[i+1]),
+ *             in the walk's order (deterministic, not sorted).  Entries past
+ *             list_cap are not written and the status word reads
+ *             BH_ETREE_OVERFLOW; call once with list = NULL to size it.
+ * Asynchronous on `stream` like bh_compute; it rebuilds the tree in the
+ * context's scratch (BH_OPT_KEY_BITS and BH_OPT_LEAF_CAP apply) and replaces
+ * the state bh_debug_export would read.  BH_EINVAL for bad arguments.
+ */
+#define BH_NB_GATHER     0
+#define BH_NB_SYMMETRIC  1
+int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
+                 float kappa, int mode, unsigned int *counts,
+                 unsigned long long *offsets, unsigned int *list, size_t list_cap,
+                 void *stream);
+
+/*
  * Per-stage milliseconds of the last bh_compute made with BH_OPT_TIMING on
  * (indices BH_STAGE_*; a stage that did not run reads 0).  Synchronises on
  * the last recorded event.  n = number of floats at ms (<= BH_NUM_STAGES).
