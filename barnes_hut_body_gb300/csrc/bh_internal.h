@@ -43,7 +43,8 @@ struct StepCtrl {
   unsigned long long walk_stats[4];        // rounds, nodes tested, nodes put
                                            // to the vote, leaf chunks
   int level_total[kMaxLevels];             // nodes per level (build scan)
-  int pad1[2];
+  unsigned int fill_ctr;                   // group tickets of a second walk
+  int pad1;
 };
 
 // Control block kept across calls.

@@ -25,11 +25,13 @@ namespace {
 
 constexpr int kNbThreads = 128;
 constexpr int kNbWarps = kNbThreads / 32;
-constexpr int kNbStack = 1024;           // node indices per warp
-// Rounds pop up to 32 nodes while 7 entries per popped node stay free beyond
-// a reserve; once the reserve is reached they pop one node (depth first),
-// which grows the stack by at most 7 per level: 7 * 22 + 8 entries.
-constexpr int kNbReserve = 7 * kMaxLevels + 8;
+// Child ranges per warp.  A round takes up to 32 nodes from the top ranges
+// (deepest first) and pushes at most 32, the ranges of the cells it opened,
+// the deepest on top, so levels never decrease towards the top.  A round
+// that takes level-l nodes has first consumed every range above them, all
+// deeper than l; so the level-(l+1) ranges on the stack all come from one
+// round: at most 32 per level, 32 * 22 + 32 = 736 < 768.
+constexpr int kNbStack = 768;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
@@ -110,6 +112,22 @@ nb_node_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
   }
 }
 
+// Can a particle in [lo, hi] with smoothing length h reach the node (true
+// also for some that cannot: the test is conservative under fp32 rounding,
+// a pair's rounded r^2 being >= d2 (1 - 2^-21))?
+__device__ __forceinline__ bool reaches(float lx, float ly, float lz, float hx, float hy,
+                                        float hz, float h, const NbNode &nd, float kappa,
+                                        bool sym) {
+  const float dx = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.x, hx), __fsub_rn(lx, nd.hi.x)));
+  const float dy = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.y, hy), __fsub_rn(ly, nd.hi.y)));
+  const float dz = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.z, hz), __fsub_rn(lz, nd.hi.z)));
+  float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
+  d2 = __fadd_rn(d2, __fmul_rn(dz, dz));
+  const float H = sym ? fmaxf(h, nd.lo_h.w) : h;
+  const float s = __fmul_rn(kappa, H);
+  return __fmul_rn(d2, 1.f - 0x1p-20f) < __fmul_rn(s, s);
+}
+
 // The exact pair test (fp32, rounded as written).
 __device__ __forceinline__ bool pair_in(const float4 &qi, float hi, const float4 &pj,
                                         float hj, float kappa, bool sym) {
@@ -122,11 +140,16 @@ __device__ __forceinline__ bool pair_in(const float4 &qi, float hi, const float4
   return r2 < __fmul_rn(s, s);
 }
 
+// Per-warp shared memory: a stack of node ranges [first, end) (children of
+// opened cells, at most 8 each), and the particle ranges of the leaves opened
+// in one round with their running offsets.
 struct NbWarp {
-  int stack[kNbStack];
+  int2 stack[kNbStack];
+  int leaf_f[32];
+  int leaf_pre[33];
 };
 
-// kFill = false: counts; true: lists at out_offs (caller order).
+// kFill = false: counts; true: lists at offs (caller order).
 template <bool kSym, bool kFill>
 __global__ void __launch_bounds__(kNbThreads)
 nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
@@ -142,9 +165,12 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
   for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
   if (nnodes > nnodes_cap) nnodes = nnodes_cap;
   const long long ngroups = (n + 31) / 32;
-  const long long gstride = (long long)gridDim.x * kNbWarps;
-  for (long long g = (long long)blockIdx.x * kNbWarps + (threadIdx.x >> 5); g < ngroups;
-       g += gstride) {
+  unsigned int *ticket = kFill ? &ctrl->step.fill_ctr : &ctrl->step.work_ctr;
+  for (;;) {
+    unsigned gg = 0;
+    if (lane == 0) gg = atomicAdd(ticket, 1u);
+    const long long g = __shfl_sync(kFull, gg, 0);
+    if (g >= ngroups) break;
     const long long qi = g * 32 + lane;
     const bool valid = qi < n;
     const float4 q = spm[valid ? qi : n - 1];
@@ -161,13 +187,16 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
       ghi_z = fmaxf(ghi_z, __shfl_xor_sync(kFull, ghi_z, o));
       ghq = fmaxf(ghq, __shfl_xor_sync(kFull, ghq, o));
     }
-    unsigned cnt = 0;
+    // a group is spread out when its box is wider than its largest search
+    // radius; then the per-particle node test pays for itself
+    const float ext = fmaxf(fmaxf(ghi_x - glo_x, ghi_y - glo_y), ghi_z - glo_z);
+    const bool spread = ext > kappa * ghq;
+    unsigned cnt = 0, tests = 0;
     unsigned long long base = 0;
     const unsigned dst = valid ? perm[qi] : 0u;
     if (kFill && valid && dst < n) base = offs[dst];
-    int sp = 0;
-    if (lane == 0 && nnodes > 0) W.stack[0] = 0;
-    sp = nnodes > 0 ? 1 : 0;
+    if (lane == 0 && nnodes > 0) W.stack[0] = make_int2(0, 1);
+    int sp = nnodes > 0 ? 1 : 0;
     __syncwarp();
     long long rounds = 0;
     while (sp > 0) {
@@ -175,64 +204,103 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
         set_err(ctrl, kErrOverflow);
         break;
       }
-      // pop k nodes; each can push at most 8 children, so keep 7k free
-      int k = sp < 32 ? sp : 32;
-      const int room = (kNbStack - kNbReserve - sp) / 7;
-      if (k > room) k = room > 0 ? room : 1;
-      const int node = lane < k ? W.stack[sp - 1 - lane] : -1;
-      sp -= k;
-      __syncwarp();
+      // up to 32 nodes from the top ranges, one per lane
+      int node = -1, got = 0;
+      while (got < 32 && sp > 0) {
+        const int2 r = W.stack[sp - 1];
+        const int len = r.y - r.x;
+        const int take = len < 32 - got ? len : 32 - got;
+        if (lane >= got && lane < got + take) node = r.x + (lane - got);
+        got += take;
+        __syncwarp();
+        if (take >= len) {
+          --sp;
+        } else if (lane == 0) {
+          W.stack[sp - 1].x = r.x + take;
+        }
+        __syncwarp();
+      }
       bool open = false, leaf = false;
       int4 t = make_int4(0, 0, -1, -1);
+      NbNode nd;
       if (node >= 0 && node < nnodes) {
         t = topo[node];
-        const NbNode nd = nodes[node];
-        const float dx = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.x, ghi_x), __fsub_rn(glo_x, nd.hi.x)));
-        const float dy = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.y, ghi_y), __fsub_rn(glo_y, nd.hi.y)));
-        const float dz = fmaxf(0.f, fmaxf(__fsub_rn(nd.lo_h.z, ghi_z), __fsub_rn(glo_z, nd.hi.z)));
-        float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
-        d2 = __fadd_rn(d2, __fmul_rn(dz, dz));
-        const float H = kSym ? fmaxf(ghq, nd.lo_h.w) : ghq;
-        const float s = __fmul_rn(kappa, H);
-        // conservative: a pair's rounded r^2 is >= d2 (1 - 2^-21)
-        open = __fmul_rn(d2, 1.f - 0x1p-20f) < __fmul_rn(s, s);
+        nd = nodes[node];
+        // first against the group's box and largest h
+        open = reaches(glo_x, glo_y, glo_z, ghi_x, ghi_y, ghi_z, ghq, nd, kappa, kSym);
         leaf = t.z < 0;
       }
-      // push the children of opened cells
-      // children lie after their parent in the breadth-first order; only
-      // such links are followed, so every walk ends
-      const bool push = open && !leaf && t.z > node && t.w > t.z && t.w <= nnodes;
-      int nch = push ? t.w - t.z : 0;
-      if (nch > 8) nch = 8;
-      int off = nch;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, off, o);
-        if (lane >= o) off += y;
+      // then, where the group is spread out, against each particle's own
+      // sphere: a node is opened only if some particle of the group can
+      // reach it
+      if (spread && __any_sync(kFull, open)) {
+        bool any = false;
+        for (int k = 0; k < 32; ++k) {
+          const float x = __shfl_sync(kFull, q.x, k), y = __shfl_sync(kFull, q.y, k),
+                      z = __shfl_sync(kFull, q.z, k), hk = __shfl_sync(kFull, hq, k);
+          const bool vk = __shfl_sync(kFull, valid, k);
+          if (open && vk && !any) any = reaches(x, y, z, x, y, z, hk, nd, kappa, kSym);
+        }
+        open = any;
       }
-      const int tot = __shfl_sync(kFull, off, 31);
-      off -= nch;
-      for (int c = 0; c < nch; ++c) {
-        if (sp + off + c < kNbStack) W.stack[sp + off + c] = t.z + c;
-        else set_err(ctrl, kErrOverflow);     // not reachable by the bound above
+      // push the child range of each opened cell; children lie after their
+      // parent in the breadth-first order and only such links are followed,
+      // so every walk ends
+      const bool push = open && !leaf && t.z > node && t.w > t.z && t.w <= nnodes &&
+                        t.w - t.z <= 8;
+      // lane 0 holds the deepest node taken; pushing in reverse lane order
+      // keeps levels non-decreasing towards the top of the stack
+      const unsigned pb = __ballot_sync(kFull, push);
+      if (push) {
+        const int at = sp + __popc(pb >> lane) - 1;
+        if (at < kNbStack) W.stack[at] = make_int2(t.z, t.w);
+        else set_err(ctrl, kErrOverflow);
       }
-      sp += tot;
+      sp += __popc(pb);
       if (sp > kNbStack) sp = kNbStack;
-      // test the particles of opened leaves
-      unsigned leaves = __ballot_sync(kFull, open && leaf);
-      while (leaves) {
-        const int src = __ffs(leaves) - 1;
-        leaves &= leaves - 1;
-        long long f = __shfl_sync(kFull, t.x, src);
-        long long e = __shfl_sync(kFull, t.y, src);
-        if (f < 0) f = 0;
-        if (e > n) e = n;
-        for (long long j = f; j < e; ++j) {
-          const float4 pj = spm[j];
-          const float hj = sh[j];
-          if (valid && j != qi && pair_in(q, hq, pj, hj, kappa, kSym)) {
+      // the particles of the opened leaves, 32 at a time (one load each)
+      const bool lf = open && leaf;
+      long long f = t.x < 0 ? 0 : t.x, e = t.y > n ? n : t.y;
+      int len = lf && e > f ? (int)(e - f) : 0;
+      int pre = len;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, pre, o);
+        if (lane >= o) pre += y;
+      }
+      const int ptot = __shfl_sync(kFull, pre, 31);
+      W.leaf_f[lane] = (int)f;
+      W.leaf_pre[lane + 1] = pre;
+      if (lane == 0) W.leaf_pre[0] = 0;
+      __syncwarp();
+      for (int c0 = 0; c0 < ptot; c0 += 32) {
+        // lane l loads particle c0 + l of the concatenated leaf ranges
+        const int pos = c0 + lane;
+        int j = -1;
+        float4 pj = make_float4(0.f, 0.f, 0.f, 0.f);
+        float hj = 0.f;
+        if (pos < ptot) {
+          int lo = 0, hi = 31;                  // last leaf with pre <= pos
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (W.leaf_pre[mid] <= pos) lo = mid; else hi = mid - 1;
+          }
+          j = W.leaf_f[lo] + (pos - W.leaf_pre[lo]);
+          pj = spm[j];
+          hj = sh[j];
+        }
+        const int m = ptot - c0 < 32 ? ptot - c0 : 32;
+        for (int k = 0; k < m; ++k) {
+          const int jk = __shfl_sync(kFull, j, k);
+          float4 pk;
+          pk.x = __shfl_sync(kFull, pj.x, k);
+          pk.y = __shfl_sync(kFull, pj.y, k);
+          pk.z = __shfl_sync(kFull, pj.z, k);
+          const float hk = __shfl_sync(kFull, hj, k);
+          tests += valid;
+          if (valid && jk != qi && pair_in(q, hq, pk, hk, kappa, kSym)) {
             if (kFill) {
               const unsigned long long at = base + cnt;
-              if (at < list_cap) list[at] = perm[j];
+              if (at < list_cap) list[at] = perm[jk];
             }
             ++cnt;
           }
@@ -246,6 +314,11 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
       } else {
         counts[dst] = cnt;
       }
+    }
+    if (!kFill) {                           // pair tests of the counting walk
+      unsigned long long tt = tests;
+      for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(kFull, tt, o);
+      if (lane == 0 && tt) atomicAdd(&ctrl->step.executed, tt);
     }
   }
 }
@@ -322,9 +395,15 @@ scan_apply(const unsigned int *__restrict__ x, long long n,
 
 template <bool kSym, bool kFill>
 cudaError_t launch_walk_t(const NbArgs &a, DevCtrl *ctrl, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nb_walk_kernel<kSym, kFill>,
+                                                  kNbThreads, 0);
+    if (per_sm < 1) per_sm = 1;
+  }
   const long long ngroups = (a.n + 31) / 32;
   long long blocks = (ngroups + kNbWarps - 1) / kNbWarps;
-  const long long cap = (long long)a.num_sms * 16;
+  const long long cap = (long long)a.num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   nb_walk_kernel<kSym, kFill><<<(unsigned)blocks, kNbThreads, 0, s>>>(

@@ -71,6 +71,10 @@ def parse():
     ap.add_argument("--stochastic", action="store_true",
                     help="time the stochastic Barnes-Hut estimator (default workload "
                          "surface2e20) beside the deterministic walk")
+    ap.add_argument("--neighbors", action="store_true",
+                    help="time the SPH neighbour search (bh_neighbors with lists) on "
+                         "a Plummer sphere with density-based smoothing lengths")
+    ap.add_argument("--nb-n", type=int, default=1 << 20)
     ap.add_argument("--samples", type=int, default=1)
     ap.add_argument("--strata-level", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
@@ -585,6 +589,83 @@ def run_stochastic(args, rank, local_rank, world):
     return 0
 
 
+def run_neighbors(args, rank, local_rank, world):
+    """SPH neighbour search: the whole bh_neighbors call (tree build, counting
+    walk, scan, list walk) on resident inputs."""
+    import ctypes
+    import numpy as np
+    import torch
+
+    import barnes_hut_body_gb300 as B
+    import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    n = args.nb_n
+    pm, h = W.sph_plummer(n, seed=4)
+    d_pm = torch.from_numpy(pm).to(device)
+    d_h = torch.from_numpy(h).to(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    bh = B.BarnesHut(device=local_rank)
+    counts, offs, lst = B.bh_neighbors(bh.ctx, d_pm, d_h, 2.0, B.BH_NB_SYMMETRIC)
+    total = int(offs[n].item())
+    L = B.lib()
+    stream = torch.cuda.current_stream(device)
+    st = ctypes.c_void_p(stream.cuda_stream)
+
+    def call(with_list=True):
+        rc = L.bh_neighbors(bh.ctx, d_pm.data_ptr(), d_h.data_ptr(), n, 2.0, B.BH_NB_SYMMETRIC,
+                            counts.data_ptr(), offs.data_ptr(),
+                            lst.data_ptr() if with_list else None,
+                            total if with_list else 0, st)
+        if rc != 0:
+            raise RuntimeError(B.bh_last_error(bh.ctx))
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    if bh.status() != 0:
+        raise RuntimeError(B.bh_last_error(bh.ctx))
+
+    def timed(with_list):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world, device)
+        torch.cuda.synchronize(device)
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            call(with_list)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(device)
+        return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
+
+    ms_count = timed(False)
+    tests, _ = B.bh_get_counters(bh.ctx)
+    ms = timed(True)
+    if bh.status() != 0:
+        raise RuntimeError(B.bh_last_error(bh.ctx))
+    c = counts.cpu().numpy()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "neighbour_pairs_per_s",
+            "value": sum_over_ranks(total, world, device) / (ms / 1e3), "unit": "pairs/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"sph_plummer n={n} (a 0.1, h from the analytic density, "
+                                   "64 neighbours within 2h on average)",
+                       "kappa": 2.0, "mode": "symmetric",
+                       "l2": "flushed (256 MiB write) before every step"},
+            "ms_counts_and_offsets_only": ms_count,
+            "pairs": total, "neighbours_per_particle": {"mean": float(c.mean()),
+                                                        "max": int(c.max())},
+            "pair_tests": tests, "tests_per_pair": tests / max(total, 1),
+            "gpu_launches": None}), flush=True)
+    bh.close()
+    return 0
+
+
 def main():
     args = parse()
     if args.workload is None:
@@ -598,6 +679,8 @@ def main():
         return run_integrate(args, rank, local_rank, world)
     if args.stochastic:
         return run_stochastic(args, rank, local_rank, world)
+    if args.neighbors:
+        return run_neighbors(args, rank, local_rank, world)
     return run_ours(args, rank, local_rank, world)
 
 

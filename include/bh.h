@@ -306,7 +306,8 @@ int bh_get_stage_times(bh_ctx *c, float *ms, int n);
  * `executed` = source terms evaluated for valid targets by the group walk
  * (stochastic estimator: monopole evaluations, i.e. one per stratum plus,
  * per surviving step, the cell's children (or particles) and the cell);
- * `groups` = number of target groups walked.
+ * `groups` = number of target groups walked.  After bh_neighbors,
+ * `executed` = pair tests of its counting walk.
  */
 int bh_get_counters(bh_ctx *c, unsigned long long *executed,
                     unsigned long long *groups);
