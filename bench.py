@@ -585,7 +585,10 @@ def run_stochastic(args, rank, local_rank, world):
             "deterministic": {"theta": theta, "ms_per_step": ms_d,
                               "evaluations_per_query": ex_d / m, "pot_abs_error": err_d},
             "error_sample": "4096 targets (PCG64 seed 7) against the direct-sum kernel",
-            "gpu_launches": None}), flush=True)
+            # per step: bbox, keys, 8 radix passes, gather, 3 build passes,
+            # centre of mass, the targets' bbox/keys/8 passes/gather, strata,
+            # stochastic walk
+            "gpu_launches": (17 if tgt is None else 28) * args.steps}), flush=True)
     return 0
 
 
@@ -661,7 +664,9 @@ def run_neighbors(args, rank, local_rank, world):
             "pairs": total, "neighbours_per_particle": {"mean": float(c.mean()),
                                                         "max": int(c.max())},
             "pair_tests": tests, "tests_per_pair": tests / max(total, 1),
-            "gpu_launches": None}), flush=True)
+            # per call: bbox, keys, 8 radix passes, gather, 3 build passes,
+            # h gather, node boxes, counting walk, 3 scan kernels, list walk
+            "gpu_launches": 21 * args.steps}), flush=True)
     bh.close()
     return 0
 
