@@ -28,6 +28,7 @@ struct bh_ctx {
   float theta = 0.5f, G = 1.f, eps = 0.f;
   int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
+  int pipeline = 0;
   unsigned long long seed = 0;
   int *strata = nullptr;
   int strata_cap = 0;
@@ -71,7 +72,7 @@ struct bh_ctx {
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
-    int estimator, samples, strata_level;
+    int estimator, samples, strata_level, pipeline;
     unsigned long long seed;
     bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
   };
@@ -271,6 +272,7 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   a.opening = c->opening;
   a.group = c->group;
   a.num_sms = c->num_sms;
+  a.pipelined = c->pipeline;
   if (c->estimator == BH_EST_STOCHASTIC) {
     SbhArgs b;
     b.spm = c->spm;
@@ -409,6 +411,9 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       if (v < 1 || v > 1024) return fail(c, BH_EINVAL, "samples must be in 1..1024");
       c->samples = (int)v;
       return BH_OK;
+    case BH_OPT_PIPELINE:
+      c->pipeline = v ? 1 : 0;
+      return BH_OK;
     case BH_OPT_STRATA_LEVEL:
       if (v < 0 || v > 6) return fail(c, BH_EINVAL, "strata level must be in 0..6");
       c->strata_level = (int)v;
@@ -474,7 +479,7 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.bits = c->bits; key.leaf_cap = c->leaf_cap; key.opening = c->opening;
   key.group = c->group; key.spin = c->spin_limit;
   key.estimator = c->estimator; key.samples = c->samples;
-  key.strata_level = c->strata_level; key.seed = c->seed;
+  key.strata_level = c->strata_level; key.seed = c->seed; key.pipeline = c->pipeline;
   bool graph = c->use_graph && !c->timing && c->cap_stream;
   if (graph) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -127,6 +127,7 @@ struct WalkArgs {
   int opening;                // BH_OPEN_*
   int group;                  // 32 or 64
   int num_sms;
+  int pipelined;              // producer/consumer warps (groups of 64)
 };
 cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s);
 

@@ -145,6 +145,15 @@ struct Acc {
 #pragma unroll 2
     for (int p = 0; p < kFlushAt / 2; ++p) pair(S.list[p][0], S.list[p][1]);
   }
+  // the same over a bare list of entry pairs
+  __device__ __forceinline__ void run_list(const ulonglong2 (*list)[2], int npairs) {
+#pragma unroll 2
+    for (int p = 0; p < npairs; ++p) pair(list[p][0], list[p][1]);
+  }
+  __device__ __forceinline__ void run_full_list(const ulonglong2 (*list)[2]) {
+#pragma unroll 2
+    for (int p = 0; p < 32; ++p) pair(list[p][0], list[p][1]);
+  }
 };
 
 // Evaluate the first kFlushAt list entries and move the rest to the front.
@@ -441,6 +450,414 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
 }
 
 
+// ---------------------------------------------------------------------------
+// Pipelined walk: the same traversal and arithmetic as walk_kernel, split
+// between two warps per group.  The producer warp traverses (pops, record
+// loads, box/probe/vote tests, leaf gathers) and fills 64-entry list buffers;
+// the consumer warp evaluates full buffers for the group's targets.  Four
+// buffers per pair circulate through two mbarriers each (full: producer ->
+// consumer, empty: consumer -> producer); every wait is bounded.  The
+// traversal (latency- and control-bound) and the evaluation (FMA-bound) of
+// different groups then overlap within an SM instead of alternating inside
+// one warp.
+// ---------------------------------------------------------------------------
+constexpr int kWsPairs = 4;
+constexpr int kWsThreads = kWsPairs * 64;
+constexpr int kWsBufs = 4;
+constexpr int kWsEntries = 64;
+constexpr unsigned kWsWaitLimit = 1u << 26;   // polls; a buffer takes microseconds
+
+struct WsHdr {
+  long long group;           // -1: no more groups
+  int n;                     // entries in the buffer
+  int last;                  // last buffer of the group
+  unsigned self0, self1;     // targets whose own particle was evaluated
+};
+
+struct WsPairSmem {
+  ulonglong2 list[kWsBufs][kWsEntries / 2][2];
+  WsHdr hdr[kWsBufs];
+  unsigned long long full[kWsBufs], empty[kWsBufs];
+  float4 cand[32];
+  float4 probe[8];
+  unsigned int stack[kStackCap];
+};
+
+__device__ __forceinline__ unsigned su32(const void *p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mb_init(unsigned long long *b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mb_arrive(unsigned long long *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mb_try(unsigned long long *b, unsigned parity) {
+  unsigned ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait by every lane; false (for the whole warp) on timeout.
+__device__ __forceinline__ bool mb_wait(unsigned long long *b, unsigned parity) {
+  bool ok = false;
+  for (unsigned i = 0; i < kWsWaitLimit && !ok; ++i) ok = mb_try(b, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void ws_put(ulonglong2 (*list)[2], int j, float4 v) {
+  float *w = reinterpret_cast<float *>(&list[j >> 1][0]);
+  const int h = j & 1;
+  w[h] = v.x;
+  w[2 + h] = v.y;
+  w[4 + h] = v.z;
+  w[6 + h] = v.w;
+}
+
+template <int T, bool kVote, bool kEps0, bool kSelf>
+__device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, WsPairSmem &S,
+                                            long long nnodes) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  constexpr int GS = 32 * T;
+  const long long ngroups = (a.m + GS - 1) / GS;
+  unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0, done = 0;
+  unsigned eph = 0;              // parity of the next wait on each empty barrier
+  int b = 0, nl = 0;
+  bool alive = mb_wait(&S.empty[0], 0);
+  eph ^= 1u;
+  // hand buffer b (nl entries) to the consumer and take the next one
+  auto hand_off = [&](long long g, int n, int last, unsigned s0, unsigned s1) {
+    if (lane == 0) {
+      WsHdr h;
+      h.group = g; h.n = n; h.last = last; h.self0 = s0; h.self1 = s1;
+      S.hdr[b] = h;
+    }
+    __syncwarp();
+    mb_arrive(&S.full[b]);
+    b = (b + 1) % kWsBufs;
+    alive = alive && mb_wait(&S.empty[b], (eph >> b) & 1u);
+    eph ^= 1u << b;
+  };
+
+  while (alive) {
+    unsigned long long gg = 0;
+    if (lane == 0) gg = atomicAdd(&ctrl->step.work_ctr, 1u);
+    const long long g = (long long)__shfl_sync(0xffffffffu, gg, 0);
+    if (g >= ngroups) break;
+    const long long t0 = g * GS;
+
+    float px[T], py[T], pz[T];
+    bool valid[T], selfhit[T];
+    float bl0 = INFINITY, bl1 = INFINITY, bl2 = INFINITY;
+    float bh0 = -INFINITY, bh1 = -INFINITY, bh2 = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < T; ++k) {
+      const long long t = t0 + k * 32 + lane;
+      valid[k] = t < a.m;
+      const float4 p = __ldg(a.tpos + (valid[k] ? t : t0));
+      px[k] = p.x; py[k] = p.y; pz[k] = p.z;
+      if ((lane & (32 / kProbesPerSlot - 1)) == 0)
+        S.probe[k * kProbesPerSlot + lane / (32 / kProbesPerSlot)] = make_float4(p.x, p.y, p.z, 0.f);
+      selfhit[k] = false;
+      bl0 = fminf(bl0, p.x); bh0 = fmaxf(bh0, p.x);
+      bl1 = fminf(bl1, p.y); bh1 = fmaxf(bh1, p.y);
+      bl2 = fminf(bl2, p.z); bh2 = fmaxf(bh2, p.z);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      bl0 = fminf(bl0, __shfl_xor_sync(0xffffffffu, bl0, o));
+      bl1 = fminf(bl1, __shfl_xor_sync(0xffffffffu, bl1, o));
+      bl2 = fminf(bl2, __shfl_xor_sync(0xffffffffu, bl2, o));
+      bh0 = fmaxf(bh0, __shfl_xor_sync(0xffffffffu, bh0, o));
+      bh1 = fmaxf(bh1, __shfl_xor_sync(0xffffffffu, bh1, o));
+      bh2 = fmaxf(bh2, __shfl_xor_sync(0xffffffffu, bh2, o));
+    }
+    int sp = 1;
+    if (lane == 0) S.stack[0] = 0u;
+    __syncwarp();
+
+    // append `cnt` entries (this lane's at rank r if put), spilling into the
+    // next buffer when the current one fills
+    auto append = [&](bool put, int r, int cnt, float4 v) {
+      if (nl + cnt > kWsEntries) {
+        const int first = kWsEntries - nl;      // entries that still fit
+        if (put && r < first) ws_put(S.list[b], nl + r, v);
+        hand_off(g, kWsEntries, 0, 0u, 0u);
+        if (put && r >= first) ws_put(S.list[b], r - first, v);
+        nl = cnt - first;
+      } else {
+        if (put) ws_put(S.list[b], nl + r, v);
+        nl += cnt;
+      }
+    };
+
+    while (sp > 0 && alive) {
+      unsigned ent = 0;
+      int cnt = 0;
+      if (lane < sp) {
+        ent = S.stack[sp - 1 - lane];
+        cnt = (int)(ent & 7u) + 1;
+      }
+      const int pre = warp_incl_scan(cnt, lane);
+      const bool take = lane < sp && pre <= 32;
+      const unsigned tmask = __ballot_sync(0xffffffffu, take);
+      const int ntake = __popc(tmask);
+      const int total = __shfl_sync(0xffffffffu, pre, ntake - 1);
+      sp -= ntake;
+      const int excl = pre - cnt;
+      const unsigned starts = __reduce_or_sync(0xffffffffu, take ? (1u << excl) : 0u);
+      bool has = lane < total;
+      int e = __popc(starts & ((2u << lane) - 1u)) - 1;
+      e = e < 0 ? 0 : e;
+      const unsigned ebase = __shfl_sync(0xffffffffu, ent >> 3, e);
+      const int eexcl = __shfl_sync(0xffffffffu, excl, e);
+      const unsigned node = ebase + (unsigned)(lane - eexcl);
+      __syncwarp();
+      ++st_rounds;
+      st_tested += (unsigned)total;
+      if (has && node >= nnodes) {
+        has = false;
+        set_err(ctrl, kErrOverflow);
+      }
+      float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (has) {
+        const float4 *r = reinterpret_cast<const float4 *>(a.rec + node);
+        c4 = __ldg(r);
+        q = __ldg(r + 1);
+      }
+      const float ro2 = q.x;
+      const int link = __float_as_int(q.y);
+      int count = __float_as_int(q.z);
+      const int flags = __float_as_int(q.w);
+      bool acc = false;
+      if (has) {
+        float dx = fmaxf(fmaxf(bl0 - c4.x, c4.x - bh0), 0.f);
+        float dy = fmaxf(fmaxf(bl1 - c4.y, c4.y - bh1), 0.f);
+        float dz = fmaxf(fmaxf(bl2 - c4.z, c4.z - bh2), 0.f);
+        acc = ro2 < fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+      }
+      if (kVote) {
+        bool und = has && !acc;
+        if (__any_sync(0xffffffffu, und)) {
+#pragma unroll
+          for (int k = 0; k < kProbesPerSlot * T; ++k) {
+            const float4 pr = S.probe[k];
+            float dx = c4.x - pr.x, dy = c4.y - pr.y, dz = c4.z - pr.z;
+            float r2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+            und = und && (ro2 < r2);
+          }
+        }
+        unsigned cand = __ballot_sync(0xffffffffu, und);
+        st_voted += __popc(cand);
+        if (und) S.cand[lane] = make_float4(c4.x, c4.y, c4.z, ro2);
+        __syncwarp();
+        unsigned accm = 0;
+        while (cand) {
+          const int c = __ffs(cand) - 1;
+          cand &= cand - 1u;
+          const float4 cd = S.cand[c];
+          bool ok = true;
+#pragma unroll
+          for (int k = 0; k < T; ++k) {
+            float dx = cd.x - px[k], dy = cd.y - py[k], dz = cd.z - pz[k];
+            float r2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+            ok = ok && (!valid[k] || cd.w < r2);
+          }
+          if (__all_sync(0xffffffffu, ok)) accm |= 1u << c;
+        }
+        acc = acc || ((accm >> lane) & 1u);
+      }
+      const bool leaf = (flags & 1) != 0;
+      const bool open_int = has && !acc && !leaf && count >= 1 && count <= 8 &&
+                            (unsigned)link > node && (long long)link + count <= nnodes;
+      const bool open_leaf = has && !acc && leaf && link >= 0 && link <= a.n;
+      if (open_leaf && count > a.n - link) count = (int)(a.n - link);
+
+      // accepted nodes -> list
+      const unsigned am = __ballot_sync(0xffffffffu, has && acc);
+      append(has && acc, __popc(am & lt), __popc(am), c4);
+
+      // opened internal nodes -> stack
+      const unsigned om = __ballot_sync(0xffffffffu, open_int);
+      const int npush = __popc(om);
+      if (sp + npush <= kStackCap) {
+        if (open_int)
+          S.stack[sp + __popc(om & lt)] = ((unsigned)link << 3) | (unsigned)(count - 1);
+        sp += npush;
+      } else if (npush) {
+        if (lane == 0) set_err(ctrl, kErrOverflow);
+      }
+      __syncwarp();
+
+      // opened leaves -> their particles
+      const unsigned lm = __ballot_sync(0xffffffffu, open_leaf);
+      if (lm) {
+        const int pc = open_leaf ? (count > 0 ? count : 0) : 0;
+        const int ppre = warp_incl_scan(pc, lane);
+        const int ptotal = __shfl_sync(0xffffffffu, ppre, 31);
+        const int pexcl = ppre - pc;
+        const bool mine = kSelf && open_leaf && pc > 0 && (long long)link < t0 + GS &&
+                          (long long)link + pc > t0;
+        if (kSelf && __any_sync(0xffffffffu, mine)) {
+          unsigned long long msk = 0ull;
+          if (mine) {
+            long long lo = (long long)link - t0, hi = lo + pc;
+            if (lo < 0) lo = 0;
+            if (hi > GS) hi = GS;
+            if (lo < hi) {
+              unsigned long long upper = (hi >= 64) ? ~0ull : ((1ull << hi) - 1ull);
+              msk = upper & ~((1ull << lo) - 1ull);
+            }
+          }
+          const unsigned m0 = __reduce_or_sync(0xffffffffu, (unsigned)msk);
+          const unsigned m1 = __reduce_or_sync(0xffffffffu, (unsigned)(msk >> 32));
+#pragma unroll
+          for (int k = 0; k < T; ++k)
+            selfhit[k] = selfhit[k] || (((k == 0 ? m0 : m1) >> lane) & 1u);
+        }
+        for (int base = 0; base < ptotal && alive; base += 32) {
+          ++st_chunks;
+          const int qi = base + lane;
+          int lo = 0;
+#pragma unroll
+          for (int s = 16; s >= 1; s >>= 1) {
+            int v = __shfl_sync(0xffffffffu, ppre, lo + s - 1);
+            if (v <= qi) lo += s;
+          }
+          const int owner = lo > 31 ? 31 : lo;
+          const int of = __shfl_sync(0xffffffffu, link, owner);
+          const int oe = __shfl_sync(0xffffffffu, pexcl, owner);
+          float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (qi < ptotal) pv = __ldg(a.spm + of + (qi - oe));
+          const int nput = (ptotal - base < 32) ? (ptotal - base) : 32;
+          append(qi < ptotal, lane, nput, pv);
+          __syncwarp();
+        }
+      }
+    }
+    if (!alive) break;
+    // the group's last buffer: pad to a pair, record the self hits
+    if ((nl & 1) && lane == 0) ws_put(S.list[b], nl, make_float4(0.f, 0.f, 0.f, 0.f));
+    const unsigned s0 = __ballot_sync(0xffffffffu, selfhit[0]);
+    const unsigned s1 = T > 1 ? __ballot_sync(0xffffffffu, selfhit[T - 1]) : 0u;
+    hand_off(g, nl, 1, s0, s1);
+    nl = 0;
+    ++done;
+  }
+  // no more groups: tell the consumer
+  if (alive) {
+    if (lane == 0) {
+      WsHdr h;
+      h.group = -1; h.n = 0; h.last = 1; h.self0 = h.self1 = 0u;
+      S.hdr[b] = h;
+    }
+    __syncwarp();
+    mb_arrive(&S.full[b]);
+  } else if (lane == 0) {
+    set_err(ctrl, kErrTimeout);
+  }
+  if (lane == 0) {
+    atomicAdd(&ctrl->step.groups, done);
+    atomicAdd(&ctrl->step.walk_stats[0], st_rounds);
+    atomicAdd(&ctrl->step.walk_stats[1], st_tested);
+    atomicAdd(&ctrl->step.walk_stats[2], st_voted);
+    atomicAdd(&ctrl->step.walk_stats[3], st_chunks);
+  }
+}
+
+template <int T, bool kEps0, bool kSelf>
+__device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, WsPairSmem &S) {
+  const int lane = threadIdx.x & 31;
+  constexpr int GS = 32 * T;
+  unsigned long long executed = 0;
+  // all buffers start empty
+#pragma unroll
+  for (int k = 0; k < kWsBufs; ++k) mb_arrive(&S.empty[k]);
+  unsigned fph = 0;
+  int b = 0;
+  long long cur = -2;
+  int nvalid = 0;
+  Acc<T, kEps0> accum;
+  accum.eps2 = pk(a.eps2, a.eps2);
+  for (;;) {
+    if (!mb_wait(&S.full[b], (fph >> b) & 1u)) {
+      if (lane == 0) set_err(ctrl, kErrTimeout);
+      break;
+    }
+    fph ^= 1u << b;
+    const WsHdr h = S.hdr[b];
+    if (h.group < 0) break;
+    if (h.group != cur) {                 // first buffer of a new group
+      cur = h.group;
+      const long long t0 = cur * GS;
+      nvalid = (int)((a.m - t0) < GS ? (a.m - t0) : GS);
+#pragma unroll
+      for (int k = 0; k < T; ++k) {
+        const long long t = t0 + k * 32 + lane;
+        const float4 p = __ldg(a.tpos + (t < a.m ? t : t0));
+        accum.px[k] = pk(p.x, p.x);
+        accum.py[k] = pk(p.y, p.y);
+        accum.pz[k] = pk(p.z, p.z);
+        accum.ax[k] = accum.ay[k] = accum.az[k] = accum.ph[k] = 0ull;
+      }
+    }
+    if (h.n > 0) {
+      if (h.n == kWsEntries) accum.run_full_list(S.list[b]);
+      else accum.run_list(S.list[b], (h.n + 1) / 2);
+      executed += (unsigned long long)h.n * nvalid;
+    }
+    if (h.last) {
+      const long long t0 = cur * GS;
+#pragma unroll
+      for (int k = 0; k < T; ++k) {
+        const long long t = t0 + k * 32 + lane;
+        if (t >= a.m) continue;
+        float x0, x1, y0, y1, z0, z1, p0, p1;
+        upk(accum.ax[k], x0, x1);
+        upk(accum.ay[k], y0, y1);
+        upk(accum.az[k], z0, z1);
+        upk(accum.ph[k], p0, p1);
+        float ph = p0 + p1;
+        const bool sh = (((k == 0 ? h.self0 : h.self1) >> lane) & 1u) != 0;
+        if (kSelf && !kEps0 && sh) {
+          const float m_self = __ldg(a.tpos + t).w;
+          ph += m_self * rsqrtf(a.eps2);
+        }
+        const unsigned ci = a.tperm ? a.tperm[t] : (unsigned)t;
+        if (ci < (unsigned long long)a.m)
+          a.out[ci] = make_float4(a.G * (x0 + x1), a.G * (y0 + y1), a.G * (z0 + z1),
+                                  a.G * ph);
+      }
+    }
+    __syncwarp();
+    mb_arrive(&S.empty[b]);
+    b = (b + 1) % kWsBufs;
+  }
+  if (lane == 0) atomicAdd(&ctrl->step.executed, executed);
+}
+
+template <int T, bool kVote, bool kEps0, bool kSelf>
+__global__ void __launch_bounds__(kWsThreads, 3)
+walk_ws_kernel(WalkArgs a, DevCtrl *ctrl) {
+  __shared__ WsPairSmem smem[kWsPairs];
+  const int w = threadIdx.x >> 5;
+  WsPairSmem &S = smem[w >> 1];
+  if (threadIdx.x < kWsPairs * kWsBufs) {
+    const int p = threadIdx.x / kWsBufs, k = threadIdx.x % kWsBufs;
+    mb_init(&smem[p].full[k], 32);
+    mb_init(&smem[p].empty[k], 32);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+  long long nnodes = 0;
+  for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  if (w & 1) ws_consumer<T, kEps0, kSelf>(a, ctrl, S);
+  else ws_producer<T, kVote, kEps0, kSelf>(a, ctrl, S, nnodes);
+}
+
 // Per-target interaction count: the number of terms a walk that decides the
 // opening test per target (no group vote) evaluates -- accepted cells plus
 // particle pairs of opened leaves, the own pair excluded.  One thread per
@@ -495,7 +912,25 @@ count_kernel(const NodeRec *__restrict__ rec, const float4 *__restrict__ tpos,
 }
 
 template <int T, bool kVote, bool kEps0, bool kSelf>
+cudaError_t launch_ws(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, walk_ws_kernel<T, kVote, kEps0, kSelf>, kWsThreads, 0);
+    if (per_sm < 1) per_sm = 1;
+  }
+  const long long ngroups = (a.m + 32 * T - 1) / (32 * T);
+  long long blocks = (long long)a.num_sms * per_sm;
+  const long long need = (ngroups + kWsPairs - 1) / kWsPairs;
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  walk_ws_kernel<T, kVote, kEps0, kSelf><<<(unsigned)blocks, kWsThreads, 0, s>>>(a, ctrl);
+  return cudaGetLastError();
+}
+
+template <int T, bool kVote, bool kEps0, bool kSelf>
 cudaError_t launch_one(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
+  if (T == 2 && a.pipelined) return launch_ws<T, kVote, kEps0, kSelf>(a, ctrl, s);
   static int per_sm = 0;
   if (per_sm == 0) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(

@@ -95,11 +95,13 @@ def test_direct_source_target():
 
 @pytest.mark.parametrize("name", ["uniform4096", "plummer_2e15", "galaxy_2e16", "ragged_12345"])
 @pytest.mark.parametrize("theta", [0.3, 0.5, 0.8])
-@pytest.mark.parametrize("group,opening", [(64, 0), (32, 0), (64, 1)])
-def test_walk_matches_oracle_group_walk(name, theta, group, opening):
+@pytest.mark.parametrize("group,opening,pipeline", [(64, 0, 0), (32, 0, 0), (64, 1, 0),
+                                                    (64, 0, 1)])
+def test_walk_matches_oracle_group_walk(name, theta, group, opening, pipeline):
     src = SETS[name]
     G, eps = 1.0, 1e-3
-    bh, got, rc = H.gpu_bh(src, theta=theta, G=G, eps=eps, group=group, opening=opening)
+    bh, got, rc = H.gpu_bh(src, theta=theta, G=G, eps=eps, group=group, opening=opening,
+                           pipeline=pipeline)
     assert rc == 0
     o = O.OracleBH(src, theta=theta, G=G, eps=eps, leaf_cap=16)
     ref, rows, _, mag = o.bh_group(group=group, mode=opening, with_abs=True)
@@ -110,6 +112,24 @@ def test_walk_matches_oracle_group_walk(name, theta, group, opening):
     H.assert_error_no_worse(got[idx], per_target, direct, name)
     ex, ng = __import__("barnes_hut_body_gb300").bh_get_counters(bh.ctx)
     assert ng == (src.shape[0] + group - 1) // group and ex > 0
+
+
+@pytest.mark.parametrize("name", ["uniform4096", "galaxy_2e16", "dups_5000", "ragged_12345"])
+@pytest.mark.parametrize("opening", [0, 1])
+def test_pipelined_walk_is_the_fused_walk_bit_for_bit(name, opening):
+    # same list order, same pairing, same arithmetic: identical results
+    src = SETS[name]
+    bh0, a, rc0 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=0)
+    bh1, b, rc1 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=1)
+    assert rc0 == 0 and rc1 == 0
+    np.testing.assert_array_equal(a, b)
+    import barnes_hut_body_gb300 as B
+    assert B.bh_get_counters(bh0.ctx) == B.bh_get_counters(bh1.ctx)
+    tgt = W.query_grid(src, side=17)
+    _, a, rc0 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=0)
+    _, b, rc1 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=1)
+    assert rc0 == 0 and rc1 == 0
+    np.testing.assert_array_equal(a, b)
 
 
 def test_theta_zero_is_the_direct_sum():
