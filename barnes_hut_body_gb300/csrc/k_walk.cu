@@ -11,8 +11,10 @@
 // order (T targets per lane):
 //  * Lane-parallel over nodes.  A shared-memory stack holds child ranges
 //    (first child, count <= 8).  Each round the warp pops ranges until it has
-//    up to 32 candidate nodes, one per lane, and loads their 32-byte records
-//    (children are contiguous, so a range is one coalesced read).
+//    up to 32 candidate nodes, one per lane, and stages their 32-byte
+//    records in shared memory with one TMA bulk copy (cp.async.bulk) per
+//    range -- children are contiguous records -- completing on a per-warp
+//    mbarrier; the wait is bounded.
 //  * Opening decision.  Every lane first tests its node against the group's
 //    bounding box: if w^2/theta^2 < d^2 with d the distance from the centre
 //    of mass to the box, the test holds for every target, so the node is
@@ -23,7 +25,8 @@
 //  * Accepted nodes (centre of mass + mass) and the particles of opened
 //    leaves are appended to a per-warp interaction list in shared memory;
 //    opened internal nodes push their child range.  Whenever 64 entries are
-//    waiting, the warp evaluates them for all its targets with Blackwell's
+//    waiting, the warp evaluates them (while the round's record copies are
+//    in flight) for all its targets with Blackwell's
 //    packed fp32x2 instructions: two entries per 64-bit operand, so a pair of
 //    entries costs two broadcast shared-memory reads and, per target, 13
 //    packed ops (3 sub, 3 fma, 3 mul, 3 fma, 1 sub) plus 2 rsqrt -- no
@@ -55,12 +58,19 @@ constexpr int kProbesPerSlot = 4;   // probe targets per 32-target slot
 // The interaction list holds entries (x, y, z, m) two by two, each pair as
 // two 16-byte words: (x_j, x_j+1, y_j, y_j+1) and (z_j, z_j+1, m_j, m_j+1).
 // One broadcast 16-byte shared load then yields two packed fp32x2 operands.
-struct WarpSmem {
+struct alignas(128) WarpSmem {
+  float4 rec[32][2];                  // the round's node records (TMA target)
   ulonglong2 list[kListCap / 2][2];
   float4 cand[32];                    // candidates put to the vote
   float4 probe[8];                    // probe targets of the group
   unsigned int stack[kStackCap];
+  unsigned long long bar;             // completion of the record copies
 };
+constexpr unsigned kRecWaitLimit = 1u << 26;   // polls; a copy takes microseconds
+
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
 
 __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
   atomicCAS(&c->keep.err, 0u, code);
@@ -195,6 +205,12 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
   unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0;
   long long nnodes = 0;
   for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  unsigned rec_phase = 0;
 
   for (;;) {
     unsigned long long g = 0;
@@ -269,20 +285,63 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       ++st_rounds;
       st_tested += (unsigned)total;
 
-      // ---- issue the candidates' record loads ----------------------------
-      if (has && node >= nnodes) {     // only after a failed earlier stage
-        has = false;
-        set_err(ctrl, kErrOverflow);
+      // ---- stage the candidates' records with TMA bulk copies -------------
+      // one copy per popped range (children are contiguous records); a
+      // range outside the node pool only follows a failed earlier stage
+      const unsigned rbase = ent >> 3;
+      const bool rok = take && (long long)rbase + cnt <= nnodes;
+      if (take && !rok) set_err(ctrl, kErrOverflow);
+      const unsigned okm = __ballot_sync(0xffffffffu, rok);
+      unsigned bytes = rok ? (unsigned)cnt * 32u : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      // the previous round's generic reads of S.rec before the async writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(smem_addr(&S.bar)), "r"(bytes) : "memory");
+      __syncwarp();
+      if (rok)
+        asm volatile(
+            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(smem_addr(&S.rec[excl][0])), "l"(a.rec + rbase), "r"((unsigned)cnt * 32u),
+              "r"(smem_addr(&S.bar)) : "memory");
+      {   // lanes whose range was refused hold no node
+        const int er = __shfl_sync(0xffffffffu, (int)rok, e);
+        if (has && (!er || !((okm >> e) & 1u))) has = false;
+      }
+      // ---- evaluate a full list while the copies are in flight ------------
+      if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
+      {
+        bool done = false;
+        for (unsigned it = 0; it < kRecWaitLimit && !done; ++it) {
+          unsigned ok;
+          asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                       " selp.u32 %0, 1, 0, p;\n}\n"
+                       : "=r"(ok) : "r"(smem_addr(&S.bar)), "r"(rec_phase) : "memory");
+          done = ok != 0;
+        }
+        rec_phase ^= 1u;
+        if (!__all_sync(0xffffffffu, done)) {
+          // give up on this launch: flag it, let the copies land, leave
+          if (lane == 0) set_err(ctrl, kErrTimeout);
+          for (unsigned it = 0; it < kRecWaitLimit; ++it) {
+            unsigned ok;
+            asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                         " selp.u32 %0, 1, 0, p;\n}\n"
+                         : "=r"(ok) : "r"(smem_addr(&S.bar)), "r"(rec_phase ^ 1u) : "memory");
+            if (ok) break;
+          }
+          return;
+        }
       }
       float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
       if (has) {
-        const float4 *r = reinterpret_cast<const float4 *>(a.rec + node);
-        c4 = __ldg(r);
-        q = __ldg(r + 1);
+        c4 = S.rec[lane][0];
+        q = S.rec[lane][1];
       }
-      // ---- evaluate a full list while the loads are in flight -------------
-      if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
 
       // ---- opening test ---------------------------------------------------
       const float ro2 = q.x;
