@@ -45,7 +45,7 @@ SM_MAX_MHZ = 2070.0
 KERNELS_PER_STEP = {21: 16, 10: 12}
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = None      # walk_kernel<2,vote>: re-captured after each change
+WALK_TRAFFIC_BYTES = 29.68e6   # walk_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
