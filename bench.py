@@ -336,20 +336,23 @@ def run_ours(args, rank, local_rank, world):
         ev[k][1].record(stream)
     torch.cuda.synchronize(device)
     graph_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
-    B.bh_set_option(bh.ctx, B.BH_OPT_TIMING, 1)
     total_useful = sum_over_ranks(useful, world, device)
     value = total_useful / (ms / 1e3)
 
-    # end to end through the host-buffer entry point (pinned memory)
+    # end to end through the host-buffer entry point (pinned memory), with
+    # the library's defaults (no per-stage events, so repeated calls replay
+    # the captured graph)
     h_src = torch.from_numpy(src).pin_memory()
     h_tgt = None if tgt is None else torch.from_numpy(tgt).pin_memory()
     h_out = torch.empty((m, 4), dtype=torch.float32).pin_memory()
-    B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
+    for _ in range(3):                   # the second identical call captures the graph
+        B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
     barrier(world, device)
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
     e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / args.e2e_steps, world, device)
+    B.bh_set_option(bh.ctx, B.BH_OPT_TIMING, 1)
     h2d = 16 * (src.shape[0] + (0 if tgt is None else tgt.shape[0]))
     d2h = 16 * m
 

@@ -68,11 +68,12 @@ typedef struct bh_ctx bh_ctx;
 #define BH_OPT_SEED          8  /* stochastic estimator: 64-bit seed (default 0) */
 #define BH_OPT_SAMPLES       9  /* stochastic estimator: paths per stratum,
                                    1..1024 (default 1)                       */
-#define BH_OPT_PIPELINE     11  /* 1: the group walk (groups of 64) runs as
-                                   producer/consumer warp pairs -- one warp
-                                   traverses and fills list buffers, the other
-                                   evaluates them; same results bit for bit.
-                                   0 (default): one warp does both          */
+#define BH_OPT_PIPELINE     11  /* 1: the group walk runs as producer/consumer
+                                   warp pairs -- one warp traverses and fills
+                                   list buffers, the other evaluates them;
+                                   same results bit for bit.  0 (default):
+                                   one warp does both for groups of 64;
+                                   groups of 32 always run as pairs         */
 #define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
                                    strata, 0..6 (default 2: up to 64 strata,
                                    the child count of the root of a tree with
