@@ -52,7 +52,7 @@ def assert_direct_close(got, ref):
         assert e.max() <= DIRECT_MAX, e.max()
 
 
-def assert_walk_close(got, ref, label="", mag=None):
+def assert_walk_close(got, ref, label="", mag=None, nterms=None, flip_rows=0):
     """Same opening rule on both sides: equal up to fp32 rounding, except
     targets where an opening decision taken in fp32 vs fp64 flips.
 
@@ -67,8 +67,19 @@ def assert_walk_close(got, ref, label="", mag=None):
         den = np.maximum(mag, 1e-3 * np.median(mag))
         ea = num / den
     e = np.maximum(ea, ep)
-    bad = e > WALK_TOL
-    assert bad.mean() <= FLIP_FRAC, (label, bad.mean(), np.sort(e)[-5:])
+    tol = WALK_TOL
+    if nterms is not None:
+        # fp32 recursive summation of n terms is exact only to about n*u of
+        # sum |term| (u = 2^-24; Higham, "Accuracy and Stability of Numerical
+        # Algorithms", section 4.2); long same-sign sums (the potential in a
+        # dense, strongly softened cluster) reach that bound
+        tol = np.maximum(WALK_TOL, np.asarray(nterms, np.float64) * 2.0 ** -24)
+    bad = e > tol
+    # flips: a decision taken in fp32 on one side and fp64 on the other
+    # changes the terms of a whole group; ``flip_rows`` lets one group flip
+    # in sets so small that a group is more than FLIP_FRAC of the rows
+    allowed = max(FLIP_FRAC * bad.size, flip_rows)
+    assert bad.sum() <= allowed, (label, bad.mean(), np.sort(e)[-5:])
     assert e.max() <= FLIP_MAX, (label, e.max())
 
 
