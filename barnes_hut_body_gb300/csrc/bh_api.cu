@@ -570,7 +570,19 @@ int bh_compute_host(bh_ctx *c, const float *pos_mass, size_t n, const float *tar
     if (!alloc_dev(c->stage_tgt, M + M / 8 + 64)) return fail(c, BH_ENOMEM, "staging");
     c->stage_m = M + M / 8 + 64;
   }
-  if (M > c->stage_o) {
+  // Page-locked (pinned) output memory is device-accessible: the kernels then
+  // write the results straight into it over the host link while they run,
+  // instead of a device buffer copied back afterwards.
+  float *dev_out = nullptr;
+  {
+    cudaPointerAttributes at;
+    if (M > 0 && cudaPointerGetAttributes(&at, acc_pot) == cudaSuccess &&
+        at.type == cudaMemoryTypeHost && at.devicePointer)
+      dev_out = reinterpret_cast<float *>(at.devicePointer);
+    else
+      cudaGetLastError();
+  }
+  if (!dev_out && M > c->stage_o) {
     cudaDeviceSynchronize();
     if (!alloc_dev(c->stage_out, M + M / 8 + 64)) return fail(c, BH_ENOMEM, "staging");
     c->stage_o = M + M / 8 + 64;
@@ -582,9 +594,9 @@ int bh_compute_host(bh_ctx *c, const float *pos_mass, size_t n, const float *tar
   if (e != cudaSuccess) return cuda_fail(c, e, "host to device copy");
   int rc = bh_compute(c, (const float *)c->stage_in, n,
                       self ? nullptr : (const float *)c->stage_tgt, m,
-                      (float *)c->stage_out, stream);
+                      dev_out ? dev_out : (float *)c->stage_out, stream);
   if (rc != BH_OK) return rc;
-  if (M > 0) {
+  if (M > 0 && !dev_out) {
     e = cudaMemcpyAsync(acc_pot, c->stage_out, sizeof(float4) * (size_t)M, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(c, e, "device to host copy");
   }

@@ -200,9 +200,11 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n,
 
 /*
  * Same as bh_compute with HOST buffers: copies the inputs to device staging
- * buffers owned by the context, computes, copies the results back and
+ * buffers owned by the context, computes, delivers the results and
  * synchronises `stream`.  Pinned (page-locked) host memory makes the copies
- * asynchronous DMA; pageable memory also works.  Returns the device status.
+ * asynchronous DMA, and a pinned acc_pot is written by the kernels directly
+ * (no copy back); pageable memory also works, through a staging buffer.
+ * Returns the device status.
  */
 int bh_compute_host(bh_ctx *c, const float *pos_mass, size_t n,
                     const float *targets, size_t m, float *acc_pot,
