@@ -151,9 +151,15 @@ struct Acc {
 #pragma unroll 2
     for (int p = 0; p < npairs; ++p) pair(S.list[p][0], S.list[p][1]);
   }
+  // unrolled 4 deep (2 with eps = 0, whose zero-distance guard would spill)
   __device__ __forceinline__ void run_full(const WarpSmem &S) {
+    if constexpr (kEps0) {
 #pragma unroll 2
-    for (int p = 0; p < kFlushAt / 2; ++p) pair(S.list[p][0], S.list[p][1]);
+      for (int p = 0; p < kFlushAt / 2; ++p) pair(S.list[p][0], S.list[p][1]);
+    } else {
+#pragma unroll 4
+      for (int p = 0; p < kFlushAt / 2; ++p) pair(S.list[p][0], S.list[p][1]);
+    }
   }
   // the same over a bare list of entry pairs
   __device__ __forceinline__ void run_list(const ulonglong2 (*list)[2], int npairs) {
@@ -161,7 +167,7 @@ struct Acc {
     for (int p = 0; p < npairs; ++p) pair(list[p][0], list[p][1]);
   }
   __device__ __forceinline__ void run_full_list(const ulonglong2 (*list)[2]) {
-#pragma unroll 2
+#pragma unroll 4
     for (int p = 0; p < 32; ++p) pair(list[p][0], list[p][1]);
   }
 };
