@@ -9,13 +9,16 @@
 //
 // Per node, a bottom-up pass stores the particles' bounding box and maximum
 // smoothing length (the last child to arrive combines its siblings, as the
-// centre-of-mass pass does).  One warp serves 32 consecutive sorted particles:
-// it tests up to 32 nodes per round (one per lane) against the group's
-// bounding box and largest smoothing length, with a margin that makes the
-// pruning conservative under fp32 rounding, pushes the children of opened
-// cells on a shared-memory stack and tests every particle of an opened leaf
-// against each lane's own particle.  A counting walk gives the counts, a scan
-// gives the offsets, and an identical second walk writes the lists.
+// centre-of-mass pass does).  One warp serves 32 consecutive sorted particles
+// (groups taken by atomic tickets): it tests up to 32 nodes per round (one per
+// lane) against the group's bounding box and largest smoothing length and,
+// when the group is spread wider than its largest search radius, against
+// each particle's own sphere -- both with a margin that makes the pruning
+// conservative under fp32 rounding -- pushes the child ranges of opened cells
+// on a shared-memory stack, and tests the particles of the round's opened
+// leaves, loaded 32 at a time, against each lane's own particle.  A counting
+// walk gives the counts, a scan gives the offsets, and an identical second
+// walk writes the lists.
 #include <climits>
 
 #include "bh_internal.h"
