@@ -25,6 +25,8 @@ BH_OK, BH_EINVAL, BH_ENOMEM, BH_ECUDA, BH_ETIMEOUT, BH_ETREE_OVERFLOW = range(6)
 BH_OPT_KEY_BITS, BH_OPT_LEAF_CAP, BH_OPT_OPENING, BH_OPT_TIMING, BH_OPT_GROUP, BH_OPT_GRAPH = 1, 2, 3, 4, 5, 6
 BH_OPT_ESTIMATOR, BH_OPT_SEED, BH_OPT_SAMPLES, BH_OPT_STRATA_LEVEL = 7, 8, 9, 10
 BH_OPT_PIPELINE = 11
+BH_OPT_ORDER = 12
+BH_ORDER_RADIX, BH_ORDER_TREE = 0, 1
 BH_EST_BARNES_HUT, BH_EST_STOCHASTIC = 0, 1
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
 BH_DBG_SPIN_LIMIT = 1
@@ -322,7 +324,7 @@ _OPTION_KEYS = dict(key_bits=BH_OPT_KEY_BITS, leaf_cap=BH_OPT_LEAF_CAP,
                     opening=BH_OPT_OPENING, timing=BH_OPT_TIMING, group=BH_OPT_GROUP,
                     graph=BH_OPT_GRAPH, estimator=BH_OPT_ESTIMATOR, seed=BH_OPT_SEED,
                     samples=BH_OPT_SAMPLES, strata_level=BH_OPT_STRATA_LEVEL,
-                    pipeline=BH_OPT_PIPELINE)
+                    pipeline=BH_OPT_PIPELINE, order=BH_OPT_ORDER)
 
 
 class BarnesHut:

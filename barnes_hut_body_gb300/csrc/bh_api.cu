@@ -29,6 +29,7 @@ struct bh_ctx {
   int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
   int pipeline = 0;
+  int order = BH_ORDER_RADIX;
   unsigned long long seed = 0;
   int *strata = nullptr;
   int strata_cap = 0;
@@ -50,6 +51,7 @@ struct bh_ctx {
   unsigned long long *status = nullptr;
   float4 *spm = nullptr, *stm = nullptr;
   BuildBufs build{};
+  OrderBufs order_bufs{};           // insertion tree of BH_ORDER_TREE
 
   double *dpartial = nullptr;
   long long dpartial_cap = 0;
@@ -72,7 +74,7 @@ struct bh_ctx {
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
-    int estimator, samples, strata_level, pipeline;
+    int estimator, samples, strata_level, pipeline, order;
     unsigned long long seed;
     bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
   };
@@ -138,6 +140,34 @@ void free_sources(bh_ctx *c) {
   free_dev(c->build.arrive); free_dev(c->build.msum); free_dev(c->build.rec);
   free_dev(c->build.tile_counts);
   c->cap_n = 0; c->cap_nodes = 0;
+}
+
+void free_order(bh_ctx *c) {
+  OrderBufs &b = c->order_bufs;
+  free_dev(b.child); free_dev(b.offs); free_dev(b.parent);
+  free_dev(b.count); free_dev(b.arrive); free_dev(b.nchn);
+  b.cap_nodes = 0;
+}
+
+// The insertion tree's pool: 2 rows + 64 nodes.  A node is a Morton (or
+// index) digit prefix that two or more rows share; the measured workloads
+// need 0.25-0.72 nodes per row, but rows that agree on long prefixes (near
+// duplicates) can need more, which the build reports as BH_ETREE_OVERFLOW.
+int ensure_order(bh_ctx *c, long long rows) {
+  const long long want = 2 * rows + 64;
+  if (want <= c->order_bufs.cap_nodes) return BH_OK;
+  cudaDeviceSynchronize();
+  free_order(c);
+  OrderBufs &b = c->order_bufs;
+  bool ok = alloc_dev(b.child, want * 8) && alloc_dev(b.offs, want * 8) &&
+            alloc_dev(b.parent, want) && alloc_dev(b.count, want) &&
+            alloc_dev(b.arrive, want) && alloc_dev(b.nchn, want);
+  if (!ok) {
+    free_order(c);
+    return fail(c, BH_ENOMEM, "insertion tree allocation failed");
+  }
+  b.cap_nodes = want;
+  return BH_OK;
 }
 
 void free_targets(bh_ctx *c) {
@@ -230,6 +260,30 @@ void record(bh_ctx *c, int i, cudaStream_t s) {
 
 namespace {
 
+// Spatial sort of n rows whose keys are in sb.keys[0] (caller order): the
+// sorted keys and indices land in sb.keys[*fb] / sb.idx[*fb] and the rows in
+// key order in `sorted`.  Radix sort then gather, or (BH_ORDER_TREE) the
+// insertion tree's depth-first order, which writes the rows itself.  Event
+// `rec` (if >= 0) is recorded between ordering and placement.
+cudaError_t enqueue_order(bh_ctx *c, const float4 *pm, long long n, SortBufs &sb,
+                          float4 *sorted, int which, int rec, int *fb, cudaStream_t s) {
+  cudaError_t e;
+  if (c->order == BH_ORDER_TREE) {
+    *fb = 1;
+    e = launch_order_tree(pm, sb.keys[0], n, c->bits, c->order_bufs, sb.keys[1], sb.idx[1],
+                          sorted, c->ctrl, c->num_sms, s);
+    if (rec >= 0) record(c, rec, s);
+    if (e == cudaSuccess)
+      e = launch_order_place(pm, sb.keys[0], n, c->bits, c->order_bufs, sb.keys[1],
+                             sb.idx[1], sorted, c->ctrl, c->num_sms, s);
+  } else {
+    e = launch_sort(sb, n, c->bits, c->ctrl, which, c->spin_limit, fb, s);
+    if (rec >= 0) record(c, rec, s);
+    if (e == cudaSuccess) e = launch_gather(pm, sb.idx[*fb], n, sorted, s);
+  }
+  return e;
+}
+
 // Enqueue every stage of one step on `s` (no host synchronisation).
 cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
                          const float4 *tg, long long M, float4 *out, bool self,
@@ -243,9 +297,8 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   record(c, 1, s);
   if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
   record(c, 2, s);
-  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
-  record(c, 3, s);
-  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
+  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->sort, c->spm, 0, 3, &fb, s);
+  else record(c, 3, s);
   record(c, 4, s);
   if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
   record(c, 5, s);
@@ -254,8 +307,7 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   if (!self) {
     if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->bits, false, s);
     if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->bits, s);
-    if (e == cudaSuccess) e = launch_sort(c->sort_t, M, c->bits, c->ctrl, 1, c->spin_limit, &fbt, s);
-    if (e == cudaSuccess) e = launch_gather(tg, c->sort_t.idx[fbt], M, c->stm, s);
+    if (e == cudaSuccess) e = enqueue_order(c, tg, M, c->sort_t, c->stm, 1, -1, &fbt, s);
   }
   record(c, 7, s);
   WalkArgs a;
@@ -343,6 +395,7 @@ int bh_destroy(bh_ctx *c) {
     cudaDeviceSynchronize();
     free_sources(c);
     free_targets(c);
+    free_order(c);
     free_dev(c->status);
     free_dev(c->strata);
     free_dev(c->nb_nodes);
@@ -414,6 +467,10 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
     case BH_OPT_PIPELINE:
       c->pipeline = v ? 1 : 0;
       return BH_OK;
+    case BH_OPT_ORDER:
+      if (v != BH_ORDER_RADIX && v != BH_ORDER_TREE) return fail(c, BH_EINVAL, "unknown order");
+      c->order = (int)v;
+      return BH_OK;
     case BH_OPT_STRATA_LEVEL:
       if (v < 0 || v > 6) return fail(c, BH_EINVAL, "strata level must be in 0..6");
       c->strata_level = (int)v;
@@ -453,6 +510,9 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   }
   if ((rc = ensure_sources(c, N)) != BH_OK) return rc;
   if (!self && (rc = ensure_targets(c, M)) != BH_OK) return rc;
+  if (c->order == BH_ORDER_TREE &&
+      (rc = ensure_order(c, c->cap_n > c->cap_m ? c->cap_n : c->cap_m)) != BH_OK)
+    return rc;
   if (c->estimator == BH_EST_STOCHASTIC && !c->strata) {
     // strata of level s <= 6 number at most 8^6
     if (!alloc_dev(c->strata, 1LL << 18)) return fail(c, BH_ENOMEM, "strata list");
@@ -480,6 +540,7 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.group = c->group; key.spin = c->spin_limit;
   key.estimator = c->estimator; key.samples = c->samples;
   key.strata_level = c->strata_level; key.seed = c->seed; key.pipeline = c->pipeline;
+  key.order = c->order;
   bool graph = c->use_graph && !c->timing && c->cap_stream;
   if (graph) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -664,6 +725,7 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
     return BH_OK;
   }
   if ((rc = ensure_sources(c, N)) != BH_OK) return rc;
+  if (c->order == BH_ORDER_TREE && (rc = ensure_order(c, c->cap_n)) != BH_OK) return rc;
   if (c->nb_cap_n < c->cap_n || c->nb_cap_nodes < c->cap_nodes) {
     cudaDeviceSynchronize();
     free_dev(c->nb_nodes); free_dev(c->nb_h); free_dev(c->nb_scan);
@@ -679,8 +741,7 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
   cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
   if (e == cudaSuccess) e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
   if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
-  if (e == cudaSuccess) e = launch_sort(c->sort, N, c->bits, c->ctrl, 0, c->spin_limit, &fb, s);
-  if (e == cudaSuccess) e = launch_gather(pm, c->sort.idx[fb], N, c->spm, s);
+  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->sort, c->spm, 0, -1, &fb, s);
   if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
   NbArgs a;
   a.spm = c->spm;

@@ -44,6 +44,8 @@ struct StepCtrl {
                                            // to the vote, leaf chunks
   int level_total[kMaxLevels];             // nodes per level (build scan)
   unsigned int fill_ctr;                   // group tickets of a second walk
+  unsigned int trie_nodes;                 // insertion tree: nodes allocated
+  unsigned int order_fail;                 // insertion tree: a row left out
   int pad1;
 };
 
@@ -94,6 +96,29 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
                         cudaStream_t s);
 cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
                           long long n, float4 *out, cudaStream_t s);
+
+// Tree-topology order (k_order.cu): an insertion tree over the Morton digits
+// then the index digits of every particle; its depth-first slot order is the
+// stable (key, index) order.
+struct OrderBufs {
+  int *child;            // 8 slots per node: EMPTY, LOCKED, -3 - particle, node
+  int *offs;             // 8 per node: start of each slot's range in the node's
+  int *parent;
+  int *count;            // particles below the node
+  int *arrive;           // children that finished counting
+  int *nchn;             // slots holding nodes
+  long long cap_nodes;
+};
+// Builds the tree over keys[0..n) (caller order) and counts it.
+cudaError_t launch_order_tree(const float4 *pm, const unsigned long long *keys, long long n,
+                              int bits, OrderBufs &b, unsigned long long *skeys,
+                              unsigned int *sidx, float4 *spm, DevCtrl *ctrl, int num_sms,
+                              cudaStream_t s);
+// Writes every particle's key, index and row at its depth-first rank.
+cudaError_t launch_order_place(const float4 *pm, const unsigned long long *keys, long long n,
+                               int bits, OrderBufs &b, unsigned long long *skeys,
+                               unsigned int *sidx, float4 *spm, DevCtrl *ctrl, int num_sms,
+                               cudaStream_t s);
 
 struct BuildBufs {
   int4 *topo;            // (first, end, first_child | -1, child_end)

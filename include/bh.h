@@ -74,10 +74,35 @@ typedef struct bh_ctx bh_ctx;
                                    same results bit for bit.  0 (default):
                                    one warp does both for groups of 64;
                                    groups of 32 always run as pairs         */
+#define BH_OPT_ORDER        12  /* spatial sort of sources and targets, see
+                                   BH_ORDER_* (default BH_ORDER_RADIX)       */
 #define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
                                    strata, 0..6 (default 2: up to 64 strata,
                                    the child count of the root of a tree with
                                    4 children per axis)                      */
+
+/*
+ * Spatial sort before the tree build (both give the same permutation, bit
+ * for bit: stable by Morton key, ties by index).
+ *
+ * BH_ORDER_RADIX: least-significant-digit radix sort of (key, index), then a
+ *   gather of the rows into key order.
+ * BH_ORDER_TREE: the order of the GASPHiA tree-code page (section "排序算法"):
+ *   an octree built by insertion (each row descends by octant, claims an
+ *   empty child slot with atomicCAS or locks a slot holding another row and
+ *   subdivides it until the two separate -- the tree page after Burtscher &
+ *   Pingali, sections "构建树结构" and "基于稠密存储的并行树构建实现方案"),
+ *   then subtree counts, and each parent hands its children consecutive
+ *   ranges of the order from the top down.  Octants follow the Morton digits,
+ *   then ten 3-bit digits of the row index, so the depth-first order is the
+ *   (key, index) order.  Its node pool (80 bytes x (2 rows + 64), allocated
+ *   at the first call that uses it) is enough for every measured workload
+ *   (0.25-0.72 nodes per row); rows sharing very long digit prefixes can
+ *   exhaust it, which bh_sync_status reports as BH_ETREE_OVERFLOW.  Measured
+ *   slower than BH_ORDER_RADIX on GB300; kept as the page's method.
+ */
+#define BH_ORDER_RADIX 0
+#define BH_ORDER_TREE  1
 
 #define BH_OPEN_VOTE  0  /* a cell is accepted for a group of targets only if
                             the opening test holds for every target of the
