@@ -146,6 +146,7 @@ void free_order(bh_ctx *c) {
   OrderBufs &b = c->order_bufs;
   free_dev(b.child); free_dev(b.offs); free_dev(b.parent);
   free_dev(b.count); free_dev(b.arrive); free_dev(b.nchn);
+  free_dev(b.dir); free_dev(b.hist);
   b.cap_nodes = 0;
 }
 
@@ -161,7 +162,8 @@ int ensure_order(bh_ctx *c, long long rows) {
   OrderBufs &b = c->order_bufs;
   bool ok = alloc_dev(b.child, want * 8) && alloc_dev(b.offs, want * 8) &&
             alloc_dev(b.parent, want) && alloc_dev(b.count, want) &&
-            alloc_dev(b.arrive, want) && alloc_dev(b.nchn, want);
+            alloc_dev(b.arrive, want) && alloc_dev(b.nchn, want) &&
+            alloc_dev(b.dir, 8 + 64 + 512 + 4096) && alloc_dev(b.hist, 4096);
   if (!ok) {
     free_order(c);
     return fail(c, BH_ENOMEM, "insertion tree allocation failed");

@@ -107,6 +107,8 @@ struct OrderBufs {
   int *count;            // particles below the node
   int *arrive;           // children that finished counting
   int *nchn;             // slots holding nodes
+  int *dir;              // node of each cell of depths 1..4 (or -1)
+  unsigned *hist;        // rows per depth-4 cell
   long long cap_nodes;
 };
 // Builds the tree over keys[0..n) (caller order) and counts it.

@@ -21,10 +21,17 @@
 //    two particles, and the depth-first order of the slots is the order of
 //    (key, index) -- the stable sort.
 //  * A slot holds EMPTY, LOCKED, a particle (-3 - index) or a node index.
+//  * A cell is a node exactly when two or more rows share its digits, so the
+//    cells of depths 1-4 are created before any insertion, from a histogram
+//    of the keys' leading 12 bits (one block numbers them breadth first and
+//    writes their slots).  Insertions then start at the deepest of these
+//    nodes on their path, read from a directory indexed by the leading
+//    digits: inserting into an empty tree instead makes every row contend
+//    for the same few top-level slots while they are being split.
 //    Only a slot holding a particle is locked (to subdivide it); an empty
 //    slot is claimed with one compare-and-swap.  The lock holder writes the
-//    new node (its eight slots, parent, the displaced particle), fences,
-//    and publishes the node index with an atomic exchange; others re-read
+//    new node (its eight slots, parent, the displaced particle) and
+//    publishes the node index with a release store; others re-read
 //    the slot (bounded: after kInsertLimit reads a particle gives up and
 //    flags BH_ETIMEOUT).  A full node pool flags BH_ETREE_OVERFLOW.
 //  * Counts bottom up without waiting: a node whose slots hold no nodes
@@ -49,6 +56,15 @@ constexpr int kLocked = -2;
 constexpr int kIndexDigits = 10;             // 3-bit digits of a < 2^30 index
 constexpr unsigned kInsertLimit = 1u << 22;  // slot reads per particle
 constexpr int kOrderThreads = 256;
+constexpr int kDirDepth = 4;                 // depths created up front
+constexpr int kDirSize = 8 + 64 + 512 + 4096;
+constexpr int kTopThreads = 1024;
+
+// Cells of depths 1..4 in breadth-first order: depth d starts at
+// dir_base(d) and holds 8^d cells, indexed by the key's leading d digits.
+__device__ __forceinline__ int dir_base(int d) {
+  return d == 1 ? 0 : d == 2 ? 8 : d == 3 ? 72 : 584;
+}
 
 __device__ __forceinline__ int enc_particle(unsigned i) { return -3 - (int)i; }
 __device__ __forceinline__ unsigned dec_particle(int c) { return (unsigned)(-3 - c); }
@@ -57,6 +73,12 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Release store: the writes before it (a new node's slots) are visible to
+// any thread whose acquire load reads the stored value.
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
@@ -79,23 +101,114 @@ __device__ __forceinline__ int digit_at(unsigned long long key, unsigned idx, in
   return (int)((idx >> (3 * (kIndexDigits - 1 - j))) & 7u);
 }
 
-__global__ void order_init_kernel(OrderBufs b, DevCtrl *ctrl) {
-  if (threadIdx.x < 8) b.child[threadIdx.x] = kEmpty;
-  if (threadIdx.x == 0) {
+// Rows per depth-4 cell (the hist array is zeroed before the call).
+__global__ void __launch_bounds__(kOrderThreads)
+order_hist_kernel(const unsigned long long *keys, long long n, int bits, unsigned *hist) {
+  __shared__ unsigned h[4096];
+  for (int k = threadIdx.x; k < 4096; k += blockDim.x) h[k] = 0u;
+  __syncthreads();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride)
+    atomicAdd(&h[(int)(keys[i] >> (3 * (bits - kDirDepth)))], 1u);
+  __syncthreads();
+  for (int k = threadIdx.x; k < 4096; k += blockDim.x)
+    if (h[k]) atomicAdd(&hist[k], h[k]);
+}
+
+// One block: the root and every cell of depths 1..4 holding two or more
+// rows become nodes 0, 1, 2, ... in breadth-first order, with their slots
+// pointing at their node children (EMPTY elsewhere: a cell of one row is
+// claimed by that row's insertion); dir[] maps each cell to its node or -1.
+__global__ void __launch_bounds__(kTopThreads)
+order_top_kernel(const unsigned *hist, OrderBufs b, DevCtrl *ctrl) {
+  __shared__ int cnt[kDirSize];
+  __shared__ int part[kTopThreads];
+  const int t = threadIdx.x;
+  for (int k = t; k < 4096; k += kTopThreads) cnt[dir_base(4) + k] = (int)hist[k];
+  __syncthreads();
+  for (int d = 3; d >= 1; --d) {
+    const int cells = 1 << (3 * d);
+    for (int k = t; k < cells; k += kTopThreads) {
+      int s = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) s += cnt[dir_base(d + 1) + 8 * k + c];
+      cnt[dir_base(d) + k] = s;
+    }
+    __syncthreads();
+  }
+  // node numbers: 1 + rank among the cells with >= 2 rows (breadth first)
+  constexpr int kPer = (kDirSize + kTopThreads - 1) / kTopThreads;
+  const int lo = t * kPer, hi = min(lo + kPer, kDirSize);
+  int mine = 0;
+  for (int k = lo; k < hi; ++k) mine += cnt[k] >= 2;
+  part[t] = mine;
+  __syncthreads();
+  for (int o = 1; o < kTopThreads; o <<= 1) {      // inclusive scan
+    const int v = t >= o ? part[t - o] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  int rank = part[t] - mine;
+  const int total = part[kTopThreads - 1];
+  __syncthreads();
+  for (int k = lo; k < hi; ++k) {   // cnt[] becomes the node number (or -1)
+    const bool node = cnt[k] >= 2;
+    cnt[k] = node ? 1 + rank : -1;
+    rank += node;
+  }
+  __syncthreads();
+  if (total + 1 > b.cap_nodes) {    // cannot happen: the pool holds 2n + 64
+    if (t == 0) {
+      atomicCAS(&ctrl->keep.err, 0u, kErrOverflow);
+      ctrl->step.order_fail = 1u;
+    }
+    return;
+  }
+  for (int k = t; k < kDirSize; k += kTopThreads) b.dir[k] = cnt[k];
+  if (t < 8) b.child[t] = cnt[t] >= 0 ? cnt[t] : kEmpty;      // the root
+  if (t == 0) {
     b.parent[0] = -1;
     b.arrive[0] = 0;
-    ctrl->step.trie_nodes = 1u;
+    ctrl->step.trie_nodes = 1u + (unsigned)total;
+  }
+  for (int k = t; k < kDirSize; k += kTopThreads) {
+    const int node = cnt[k];
+    if (node < 0) continue;
+    const int d = k < 8 ? 1 : k < 72 ? 2 : k < 584 ? 3 : 4;
+    const int local = k - dir_base(d);
+    b.parent[node] = d == 1 ? 0 : cnt[dir_base(d - 1) + (local >> 3)];
+    b.arrive[node] = 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int ch = d < kDirDepth ? cnt[dir_base(d + 1) + 8 * local + c] : -1;
+      b.child[(long long)node * 8 + c] = ch >= 0 ? ch : kEmpty;
+    }
   }
 }
 
 __global__ void __launch_bounds__(kOrderThreads)
 order_insert_kernel(const unsigned long long *keys, long long n, int bits, OrderBufs b,
                     DevCtrl *ctrl) {
+  // the top levels were not set up (pool too small): nothing to insert into
+  if (*(volatile const unsigned *)&ctrl->step.order_fail) return;
+  __shared__ int dir[kDirSize];
+  for (int k = threadIdx.x; k < kDirSize; k += blockDim.x) dir[k] = b.dir[k];
+  __syncthreads();
   const int max_depth = bits + kIndexDigits;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
     const unsigned long long key = keys[i];
     int node = 0, depth = 0;
+#pragma unroll
+    for (int d = kDirDepth; d >= 1; --d) {       // deepest node on the path
+      const int v = dir[dir_base(d) + (int)(key >> (3 * (bits - d)))];
+      if (v >= 0) {
+        node = v;
+        depth = d;
+        break;
+      }
+    }
     unsigned reads = 0;
     for (;;) {
       if (++reads > kInsertLimit) {
@@ -137,8 +250,9 @@ order_insert_kernel(const unsigned long long *keys, long long n, int bits, Order
       b.parent[nn] = node;
       b.arrive[nn] = 0;
       nc[digit_at(keys[j], j, d1 + 1, bits)] = c;
-      __threadfence();
-      atomicExch(slot, (int)nn);
+      // the slot is locked by this thread: no other thread writes it, so a
+      // release store publishes the node
+      st_release(slot, (int)nn);
       node = (int)nn;
       depth = d1;
     }
@@ -254,8 +368,11 @@ cudaError_t launch_order_tree(const float4 *pm, const unsigned long long *keys, 
                               unsigned int *sidx, float4 *spm, DevCtrl *ctrl, int num_sms,
                               cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  order_init_kernel<<<1, 32, 0, s>>>(b, ctrl);
+  cudaError_t e = cudaMemsetAsync(b.hist, 0, 4096 * sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
   const int gp = grid_for(n, num_sms);
+  order_hist_kernel<<<gp, kOrderThreads, 0, s>>>(keys, n, bits, b.hist);
+  order_top_kernel<<<1, kTopThreads, 0, s>>>(b.hist, b, ctrl);
   order_insert_kernel<<<gp, kOrderThreads, 0, s>>>(keys, n, bits, b, ctrl);
   // the node passes stride up to the count the insertion left on the device
   long long nodes = n < b.cap_nodes ? n : b.cap_nodes;

@@ -43,9 +43,16 @@ FLOPS_PER_TERM = 20
 # (FMA) x 2070 MHz (maximum SM clock).
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
-# Our kernels per self-mode step with 63-bit keys: bbox, keys, 8 radix passes,
-# gather, build count/scan/write, centre of mass, walk.
+# Our kernels per step with 63-bit keys: per particle set bbox, keys and the
+# order (8 radix passes + gather, or the tree order's init, insert, node
+# count, count and place kernels); then build count/scan/write, centre of
+# mass and walk.
 KERNELS_PER_STEP = {21: 16, 10: 12}
+
+
+def kernels_per_step(order: str, self_mode: bool) -> int:
+    per_set = 2 + (9 if order == "radix" else 5)
+    return per_set * (1 if self_mode else 2) + 5
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 29.68e6   # walk_kernel<2,vote> on lattice1m_shuffled, from that capture
@@ -81,6 +88,9 @@ def parse():
     ap.add_argument("--samples", type=int, default=1)
     ap.add_argument("--strata-level", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--order", choices=["radix", "tree"], default="radix",
+                    help="spatial sort: radix sort (default) or the tree-topology order "
+                         "of an insertion-built tree (BH_ORDER_TREE)")
     return ap.parse_args()
 
 
@@ -225,7 +235,7 @@ def run_reference(args, rank, world):
         "unit": "interactions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args.workload, src, tgt, theta, eps),
+        "config": workload_config(args.workload, src, tgt, theta, eps, args.order),
         "cpu_baseline": {"value": value, "unit": "interactions/s", "cores": O.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "interactions/s", "h2d_bytes_per_step": 0,
@@ -245,27 +255,34 @@ def measured_hbm_gbs() -> float:
         return 6800.0
 
 
-def stage_bytes(n: int, m: int, nodes: int, self_mode: bool) -> dict:
+def stage_bytes(n: int, m: int, nodes: int, self_mode: bool, order: str = "radix") -> dict:
     """Algorithmic DRAM bytes of each build-side stage for one step (63-bit
-    keys, 8 radix passes): what the stage must read and write at least."""
+    keys, 8 radix passes): what the stage must read and write at least.
+    The tree order's "sort" is the insertion tree: keys read, and per row at
+    least one 4-byte child slot written and its count and offset settled
+    (12 bytes); its "reorder" reads keys and rows and writes the sorted key,
+    index and row (8 + 16 in, 8 + 4 + 16 out)."""
+    sort = 8 * 24 * n if order == "radix" else 8 * n + 12 * n
+    reorder = 4 * n + 16 * n + 16 * n if order == "radix" else 24 * n + 28 * n
     b = {
         "bbox": 16 * n,                          # read particles
         "keys": 16 * n + 8 * n,                  # read particles, write keys
-        "sort": 8 * 24 * n,                      # per pass: key+index in and out
-        "reorder": 4 * n + 16 * n + 16 * n,      # perm, gather, write
+        "sort": sort,                            # radix: per pass key+index in and out
+        "reorder": reorder,                      # radix: perm, gather, write
         "build": 2 * 8 * n + 25 * nodes,         # keys twice; topology written
         "com": 16 * n + 69 * nodes,              # particles; topology in, records out
     }
     if not self_mode:
-        b["targets"] = 16 * m + 24 * m + 8 * 24 * m + 36 * m
+        tsort = 8 * 24 * m + 36 * m if order == "radix" else 20 * m + 52 * m
+        b["targets"] = 16 * m + 24 * m + tsort
     return b
 
 
-def workload_config(name, src, tgt, theta, eps):
+def workload_config(name, src, tgt, theta, eps, order="radix"):
     return {"workload": name, "n_sources": int(src.shape[0]),
             "n_targets": int(src.shape[0] if tgt is None else tgt.shape[0]),
             "theta": theta, "eps": eps, "opening": "warp vote, groups of 64",
-            "leaf_cap": 16, "key_bits": 63,
+            "leaf_cap": 16, "key_bits": 63, "order": order,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
 
 
@@ -291,7 +308,8 @@ def run_ours(args, rank, local_rank, world):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1)
+    order = B.BH_ORDER_TREE if args.order == "tree" else B.BH_ORDER_RADIX
+    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1, order=order)
     for _ in range(max(args.warmup, 3)):
         bh.compute(d_src, d_tgt, d_out)
     rc = bh.status()
@@ -369,14 +387,14 @@ def run_ours(args, rank, local_rank, world):
     stages = {k: statistics.median([s[k] for s in stage_ms]) for k in stage_ms[0]}
     walk_ms = stages["traverse"]
     nodes = int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_NODE_COUNT)[0])
-    sbytes = stage_bytes(src.shape[0], m, nodes, tgt is None)
+    sbytes = stage_bytes(src.shape[0], m, nodes, tgt is None, args.order)
     hbm_peak = measured_hbm_gbs()
     stage_gbs = {k: sbytes[k] / (stages[k] * 1e-3) / 1e9 for k in sbytes if stages.get(k, 0) > 0}
     exec_terms = statistics.median(executed)
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     achieved = exec_terms * FLOPS_PER_TERM / (walk_ms / 1e3) / 1e12
-    launches = KERNELS_PER_STEP[21] * args.steps
+    launches = kernels_per_step(args.order, tgt is None) * args.steps
 
     if rank == 0:
         cpu = None
@@ -392,7 +410,7 @@ def run_ours(args, rank, local_rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(args.workload, src, tgt, theta, eps),
+            "config": workload_config(args.workload, src, tgt, theta, eps, args.order),
             "eager_ms_per_step": eager_ms,
             "stage_ms": {k: round(v, 4) for k, v in stages.items()},
             "useful_per_step": useful, "executed_per_step": exec_terms, "nodes": nodes,
