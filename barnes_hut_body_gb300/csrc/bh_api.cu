@@ -30,6 +30,7 @@ struct bh_ctx {
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
   int pipeline = 0;
   int order = BH_ORDER_RADIX;
+  int shards = 1, shard = 0;        // walk only shard `shard` of `shards`
   unsigned long long seed = 0;
   int *strata = nullptr;
   int strata_cap = 0;
@@ -74,7 +75,7 @@ struct bh_ctx {
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
-    int estimator, samples, strata_level, pipeline, order;
+    int estimator, samples, strata_level, pipeline, order, shards, shard;
     unsigned long long seed;
     bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
   };
@@ -327,6 +328,13 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   a.group = c->group;
   a.num_sms = c->num_sms;
   a.pipelined = c->pipeline;
+  {
+    // the walk order's groups, split into `shards` contiguous ranges
+    const long long gs = c->estimator == BH_EST_STOCHASTIC ? 32 : c->group;
+    const long long ng = (M + gs - 1) / gs;
+    a.g_begin = ng * c->shard / c->shards;
+    a.g_end = ng * (c->shard + 1) / c->shards;
+  }
   if (c->estimator == BH_EST_STOCHASTIC) {
     SbhArgs b;
     b.spm = c->spm;
@@ -346,6 +354,8 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
     b.samples = c->samples;
     b.num_sms = c->num_sms;
     b.seed = c->seed;
+    b.g_begin = a.g_begin;
+    b.g_end = a.g_end;
     if (e == cudaSuccess) e = launch_sbh(b, c->strata, c->strata_cap, c->ctrl, s);
   } else if (e == cudaSuccess) {
     e = launch_walk(a, c->ctrl, s);
@@ -469,6 +479,15 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
     case BH_OPT_PIPELINE:
       c->pipeline = v ? 1 : 0;
       return BH_OK;
+    case BH_OPT_SHARDS:
+      if (v < 1 || v > (1 << 20)) return fail(c, BH_EINVAL, "shards must be in 1..2^20");
+      c->shards = (int)v;
+      if (c->shard >= c->shards) c->shard = 0;
+      return BH_OK;
+    case BH_OPT_SHARD:
+      if (v < 0 || v >= c->shards) return fail(c, BH_EINVAL, "shard must be in 0..shards-1");
+      c->shard = (int)v;
+      return BH_OK;
     case BH_OPT_ORDER:
       if (v != BH_ORDER_RADIX && v != BH_ORDER_TREE) return fail(c, BH_EINVAL, "unknown order");
       c->order = (int)v;
@@ -543,6 +562,7 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.estimator = c->estimator; key.samples = c->samples;
   key.strata_level = c->strata_level; key.seed = c->seed; key.pipeline = c->pipeline;
   key.order = c->order;
+  key.shards = c->shards; key.shard = c->shard;
   bool graph = c->use_graph && !c->timing && c->cap_stream;
   if (graph) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

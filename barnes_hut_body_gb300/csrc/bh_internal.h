@@ -155,6 +155,7 @@ struct WalkArgs {
   int group;                  // 32 or 64
   int num_sms;
   int pipelined;              // producer/consumer warps (groups of 64)
+  long long g_begin, g_end;   // the groups this call walks (a shard of them)
 };
 cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s);
 
@@ -176,6 +177,7 @@ struct SbhArgs {
   int samples;
   int num_sms;
   unsigned long long seed;
+  long long g_begin, g_end;   // groups of 32 queries this call walks
 };
 cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
                        DevCtrl *ctrl, cudaStream_t s);

@@ -174,14 +174,14 @@ __global__ void __launch_bounds__(kSbhThreads) sbh_kernel(SbhArgs a, DevCtrl *ct
   const long long ns = ctrl->step.strata;
   const long long S = a.samples;
   const long long npairs = ns * S;
-  const long long ngroups = (a.m + 31) / 32;
+  const long long gend = a.g_end;       // groups [g_begin, g_end) of this call
   const float inv_s = 1.f / (float)S;
   unsigned long long useful = 0, groups = 0;
   for (;;) {
     unsigned g = 0;
     if (lane == 0) g = atomicAdd(&ctrl->step.work_ctr, 1u);
-    g = __shfl_sync(kFull, g, 0);
-    if ((long long)g >= ngroups) break;
+    g = __shfl_sync(kFull, g, 0) + (unsigned)a.g_begin;
+    if ((long long)g >= gend) break;
     ++groups;
     const long long qi = (long long)g * 32 + lane;
     const bool valid = qi < a.m;
@@ -342,7 +342,7 @@ cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[k], sbh_kernel<false>, kSbhThreads, 0);
     if (per_sm[k] < 1) per_sm[k] = 1;
   }
-  const long long ngroups = (a.m + 31) / 32;
+  const long long ngroups = a.g_end - a.g_begin;
   long long blocks = (long long)a.num_sms * per_sm[k];
   const long long need = (ngroups + kSbhThreads / 32 - 1) / (kSbhThreads / 32);
   if (blocks > need) blocks = need;

@@ -206,7 +206,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
   WarpSmem &S = smem[threadIdx.x >> 5];
   const unsigned lt = (1u << lane) - 1u;
   constexpr int GS = 32 * T;
-  const long long ngroups = (a.m + GS - 1) / GS;
+  const long long gend = a.g_end;       // groups [g_begin, g_end) of this call
   unsigned long long executed = 0, ngroup_done = 0;
   unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0;
   long long nnodes = 0;
@@ -221,8 +221,8 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
   for (;;) {
     unsigned long long g = 0;
     if (lane == 0) g = atomicAdd(&ctrl->step.work_ctr, 1u);
-    g = __shfl_sync(0xffffffffu, g, 0);
-    if ((long long)g >= ngroups) break;
+    g = __shfl_sync(0xffffffffu, g, 0) + (unsigned long long)a.g_begin;
+    if ((long long)g >= gend) break;
     const long long t0 = (long long)g * GS;
     const int nvalid = (int)((a.m - t0) < GS ? (a.m - t0) : GS);
 
@@ -586,7 +586,7 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   constexpr int GS = 32 * T;
-  const long long ngroups = (a.m + GS - 1) / GS;
+  const long long gend = a.g_end;       // groups [g_begin, g_end) of this call
   unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0, done = 0;
   unsigned eph = 0;              // parity of the next wait on each empty barrier
   int b = 0, nl = 0;
@@ -609,8 +609,8 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
   while (alive) {
     unsigned long long gg = 0;
     if (lane == 0) gg = atomicAdd(&ctrl->step.work_ctr, 1u);
-    const long long g = (long long)__shfl_sync(0xffffffffu, gg, 0);
-    if (g >= ngroups) break;
+    const long long g = (long long)__shfl_sync(0xffffffffu, gg, 0) + a.g_begin;
+    if (g >= gend) break;
     const long long t0 = g * GS;
 
     float px[T], py[T], pz[T];
@@ -984,7 +984,7 @@ cudaError_t launch_ws(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
         &per_sm, walk_ws_kernel<T, kVote, kEps0, kSelf>, kWsThreads, 0);
     if (per_sm < 1) per_sm = 1;
   }
-  const long long ngroups = (a.m + 32 * T - 1) / (32 * T);
+  const long long ngroups = a.g_end - a.g_begin;
   long long blocks = (long long)a.num_sms * per_sm;
   const long long need = (ngroups + kWsPairs - 1) / kWsPairs;
   if (blocks > need) blocks = need;
@@ -1008,7 +1008,7 @@ cudaError_t launch_one(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
         &per_sm, walk_kernel<T, kVote, kEps0, kSelf>, kWalkThreads, 0);
     if (per_sm < 1) per_sm = 1;
   }
-  const long long ngroups = (a.m + 32 * T - 1) / (32 * T);
+  const long long ngroups = a.g_end - a.g_begin;
   long long blocks = (long long)a.num_sms * per_sm;
   long long need = (ngroups + kWalkWarps - 1) / kWalkWarps;
   if (blocks > need) blocks = need;
@@ -1048,7 +1048,7 @@ cudaError_t launch_count(const WalkArgs &a, unsigned int *counts, DevCtrl *ctrl,
 }
 
 cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
-  if (a.m <= 0) return cudaSuccess;
+  if (a.m <= 0 || a.g_end <= a.g_begin) return cudaSuccess;
   return a.group == 32 ? launch_t<1>(a, ctrl, s) : launch_t<2>(a, ctrl, s);
 }
 

@@ -76,6 +76,10 @@ typedef struct bh_ctx bh_ctx;
                                    groups of 32 always run as pairs         */
 #define BH_OPT_ORDER        12  /* spatial sort of sources and targets, see
                                    BH_ORDER_* (default BH_ORDER_RADIX)       */
+#define BH_OPT_SHARDS       13  /* split the walk into this many shards,
+                                   1..2^20 (default 1), see below            */
+#define BH_OPT_SHARD        14  /* the shard the context's calls walk,
+                                   0..shards-1 (default 0)                   */
 #define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
                                    strata, 0..6 (default 2: up to 64 strata,
                                    the child count of the root of a tree with
@@ -100,6 +104,18 @@ typedef struct bh_ctx bh_ctx;
  *   (0.25-0.72 nodes per row); rows sharing very long digit prefixes can
  *   exhaust it, which bh_sync_status reports as BH_ETREE_OVERFLOW.  Measured
  *   slower than BH_ORDER_RADIX on GB300; kept as the page's method.
+ */
+/*
+ * Shards.  The walk visits the targets in Morton order, in groups (of
+ * BH_OPT_GROUP targets; of 32 for the stochastic estimator).  With
+ * BH_OPT_SHARDS = S and BH_OPT_SHARD = s, a call still builds the whole tree
+ * and orders all targets, but walks only the groups [G s / S, G (s+1) / S)
+ * (G = number of groups, integer division) and writes only those targets'
+ * rows of acc_pot; the other rows are left as they were.  Every shard sees
+ * the same tree and the same groups, so the rows written by shards 0..S-1 of
+ * one input are the whole call's results bit for bit.  It is the split of
+ * the work over GPUs with the sources (and targets) replicated, each GPU
+ * walking one shard; the GASPHiA pages run on one GPU and have no such step.
  */
 #define BH_ORDER_RADIX 0
 #define BH_ORDER_TREE  1
