@@ -62,7 +62,7 @@ direct_kernel(const float4 *__restrict__ src, long long n,
       for (int k = 0; k < kDirT; ++k) {
         float dx = e.x - px[k], dy = e.y - py[k], dz = e.z - pz[k];
         float r2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, eps2)));
-        float inv = rsqrtf(r2);
+        float inv = rsqrt_ftz(r2);
         if (kEps0) inv = (r2 > 0.f) ? inv : 0.f;
         float minv = e.w * inv;
         float minv3 = minv * (inv * inv);
@@ -77,7 +77,7 @@ direct_kernel(const float4 *__restrict__ src, long long n,
       // self mode: the target's own row was in this tile and added
       // m*rsqrt(eps^2) to -phi (and nothing to a); take it back out
       if (kSelf && !kEps0 && ti[k] >= b && ti[k] < b + cnt)
-        fp[k] += pm[k] * rsqrtf(eps2);
+        fp[k] += pm[k] * rsqrt_ftz(eps2);
       acc[k][0] += fx[k]; acc[k][1] += fy[k];
       acc[k][2] += fz[k]; acc[k][3] += fp[k];
     }

@@ -96,7 +96,7 @@ __device__ __forceinline__ float4 mono(const float4 &q, float sx, float sy,
                                        float sz, float m, float eps2) {
   const float dx = sx - q.x, dy = sy - q.y, dz = sz - q.z;
   const float r2 = fmaf(dx, dx, fmaf(dy, dy, fmaf(dz, dz, eps2)));
-  const float inv = r2 > 0.f ? rsqrtf(r2) : 0.f;
+  const float inv = r2 > 0.f ? rsqrt_ftz(r2) : 0.f;
   const float mi = m * inv;
   const float mi3 = mi * inv * inv;
   return make_float4(mi3 * dx, mi3 * dy, mi3 * dz, -mi);

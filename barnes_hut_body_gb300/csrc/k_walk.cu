@@ -131,7 +131,7 @@ struct Acc {
       f2 r2 = fma2(dx, dx, fma2(dy, dy, fma2(dz, dz, eps2)));
       float r0, r1;
       upk(r2, r0, r1);
-      float i0 = rsqrtf(r0), i1 = rsqrtf(r1);
+      float i0 = rsqrt_ftz(r0), i1 = rsqrt_ftz(r1);
       if (kEps0) {
         i0 = (r0 > 0.f) ? i0 : 0.f;
         i1 = (r1 > 0.f) ? i1 : 0.f;
@@ -495,7 +495,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       if (kSelf && !kEps0 && selfhit[k]) {
         // undo the self pair: it added m * rsqrt(eps^2) to -phi
         const float m_self = __ldg(a.tpos + t).w;
-        ph += m_self * rsqrtf(a.eps2);
+        ph += m_self * rsqrt_ftz(a.eps2);
       }
       const unsigned ci = a.tperm ? a.tperm[t] : (unsigned)t;
       if (ci < (unsigned long long)a.m)
@@ -889,7 +889,7 @@ __device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, Ws
         const bool sh = (((k == 0 ? h.self0 : h.self1) >> lane) & 1u) != 0;
         if (kSelf && !kEps0 && sh) {
           const float m_self = __ldg(a.tpos + t).w;
-          ph += m_self * rsqrtf(a.eps2);
+          ph += m_self * rsqrt_ftz(a.eps2);
         }
         const unsigned ci = a.tperm ? a.tperm[t] : (unsigned)t;
         if (ci < (unsigned long long)a.m)
