@@ -55,7 +55,7 @@ def kernels_per_step(order: str, self_mode: bool) -> int:
     return per_set * (1 if self_mode else 2) + 5
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = None   # the kernel changed since the last capture
+WALK_TRAFFIC_BYTES = 29.68e6   # walk_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
