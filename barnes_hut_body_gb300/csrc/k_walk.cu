@@ -76,32 +76,6 @@ __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
   atomicCAS(&c->keep.err, 0u, code);
 }
 
-// ---- packed fp32x2 arithmetic (two fp32 lanes per 64-bit register) -------
-typedef unsigned long long f2;
-__device__ __forceinline__ f2 pk(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void upk(f2 v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
-  f2 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
 // Append entry j (x, y, z, m) to the paired list.
 __device__ __forceinline__ void list_put(WarpSmem &S, int j, float4 v) {
   float *w = reinterpret_cast<float *>(&S.list[j >> 1][0]);
