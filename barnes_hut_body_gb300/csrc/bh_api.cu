@@ -28,7 +28,7 @@ struct bh_ctx {
   float theta = 0.5f, G = 1.f, eps = 0.f;
   int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
-  int pipeline = 0;
+  int pipeline = 1;
   int order = BH_ORDER_RADIX;
   int shards = 1, shard = 0;        // walk only shard `shard` of `shards`
   unsigned long long seed = 0;

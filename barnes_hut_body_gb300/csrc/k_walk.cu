@@ -498,7 +498,9 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
 // consumer, empty: consumer -> producer); every wait is bounded.  The
 // traversal (latency- and control-bound) and the evaluation (FMA-bound) of
 // different groups then overlap within an SM instead of alternating inside
-// one warp.
+// one warp.  Split this way each warp needs fewer registers (64: four blocks
+// of eight warps per SM, twice the fused walk's warps), which is what makes
+// it the faster form.
 // ---------------------------------------------------------------------------
 constexpr int kWsPairs = 4;
 constexpr int kWsThreads = kWsPairs * 64;
@@ -879,7 +881,7 @@ __device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, Ws
 }
 
 template <int T, bool kVote, bool kEps0, bool kSelf>
-__global__ void __launch_bounds__(kWsThreads, 3)
+__global__ void __launch_bounds__(kWsThreads, 4)
 walk_ws_kernel(WalkArgs a, DevCtrl *ctrl) {
   __shared__ WsPairSmem smem[kWsPairs];
   const int w = threadIdx.x >> 5;

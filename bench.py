@@ -55,7 +55,7 @@ def kernels_per_step(order: str, self_mode: bool) -> int:
     return per_set * (1 if self_mode else 2) + 5
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = 29.68e6   # walk_kernel<2,vote> on lattice1m_shuffled, from that capture
+WALK_TRAFFIC_BYTES = 29.70e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -88,6 +88,9 @@ def parse():
     ap.add_argument("--samples", type=int, default=1)
     ap.add_argument("--strata-level", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--fused-walk", action="store_true",
+                    help="one warp per group both traverses and evaluates (BH_OPT_PIPELINE 0) "
+                         "instead of the default producer/consumer warp pairs")
     ap.add_argument("--order", choices=["radix", "tree"], default="radix",
                     help="spatial sort: radix sort (default) or the tree-topology order "
                          "of an insertion-built tree (BH_ORDER_TREE)")
@@ -235,7 +238,8 @@ def run_reference(args, rank, world):
         "unit": "interactions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args.workload, src, tgt, theta, eps, args.order),
+        "config": workload_config(args.workload, src, tgt, theta, eps, args.order,
+                                  args.fused_walk),
         "cpu_baseline": {"value": value, "unit": "interactions/s", "cores": O.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "interactions/s", "h2d_bytes_per_step": 0,
@@ -278,10 +282,11 @@ def stage_bytes(n: int, m: int, nodes: int, self_mode: bool, order: str = "radix
     return b
 
 
-def workload_config(name, src, tgt, theta, eps, order="radix"):
+def workload_config(name, src, tgt, theta, eps, order="radix", fused=False):
     return {"workload": name, "n_sources": int(src.shape[0]),
             "n_targets": int(src.shape[0] if tgt is None else tgt.shape[0]),
             "theta": theta, "eps": eps, "opening": "warp vote, groups of 64",
+            "walk": "fused" if fused else "producer/consumer warp pairs",
             "leaf_cap": 16, "key_bits": 63, "order": order,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
 
@@ -309,7 +314,8 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.current_stream(device)
 
     order = B.BH_ORDER_TREE if args.order == "tree" else B.BH_ORDER_RADIX
-    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1, order=order)
+    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1, order=order,
+                     pipeline=0 if args.fused_walk else 1)
     for _ in range(max(args.warmup, 3)):
         bh.compute(d_src, d_tgt, d_out)
     rc = bh.status()
@@ -388,6 +394,8 @@ def run_ours(args, rank, local_rank, world):
     walk_ms = stages["traverse"]
     nodes = int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_NODE_COUNT)[0])
     sbytes = stage_bytes(src.shape[0], m, nodes, tgt is None, args.order)
+    traffic = WALK_TRAFFIC_BYTES if (not args.fused_walk and args.order == "radix"
+                                     and args.workload == "lattice1m_shuffled") else None
     hbm_peak = measured_hbm_gbs()
     stage_gbs = {k: sbytes[k] / (stages[k] * 1e-3) / 1e9 for k in sbytes if stages.get(k, 0) > 0}
     exec_terms = statistics.median(executed)
@@ -410,7 +418,8 @@ def run_ours(args, rank, local_rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(args.workload, src, tgt, theta, eps, args.order),
+            "config": workload_config(args.workload, src, tgt, theta, eps, args.order,
+                                      args.fused_walk),
             "eager_ms_per_step": eager_ms,
             "stage_ms": {k: round(v, 4) for k, v in stages.items()},
             "useful_per_step": useful, "executed_per_step": exec_terms, "nodes": nodes,
@@ -419,8 +428,9 @@ def run_ours(args, rank, local_rank, world):
                           "frac": {k: round(v / hbm_peak, 3) for k, v in stage_gbs.items()}},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": WALK_TRAFFIC_BYTES,
-                         "kernel": "walk_kernel<2,vote>",
+                         "traffic": traffic,
+                         "kernel": "walk_kernel<2,vote>" if args.fused_walk
+                                   else "walk_ws_kernel<2,vote>",
                          "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz"},
             "e2e": {"value": total_useful / (e2e_ms / 1e3), "unit": "interactions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

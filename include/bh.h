@@ -68,12 +68,13 @@ typedef struct bh_ctx bh_ctx;
 #define BH_OPT_SEED          8  /* stochastic estimator: 64-bit seed (default 0) */
 #define BH_OPT_SAMPLES       9  /* stochastic estimator: paths per stratum,
                                    1..1024 (default 1)                       */
-#define BH_OPT_PIPELINE     11  /* 1: the group walk runs as producer/consumer
-                                   warp pairs -- one warp traverses and fills
-                                   list buffers, the other evaluates them;
-                                   same results bit for bit.  0 (default):
-                                   one warp does both for groups of 64;
-                                   groups of 32 always run as pairs         */
+#define BH_OPT_PIPELINE     11  /* 1 (default): the group walk runs as
+                                   producer/consumer warp pairs -- one warp
+                                   traverses and fills list buffers, the
+                                   other evaluates them (32 warps per SM);
+                                   0: one warp does both for groups of 64
+                                   (16 warps per SM); same results bit for
+                                   bit.  Groups of 32 always run as pairs   */
 #define BH_OPT_ORDER        12  /* spatial sort of sources and targets, see
                                    BH_ORDER_* (default BH_ORDER_RADIX)       */
 #define BH_OPT_SHARDS       13  /* split the walk into this many shards,
