@@ -13,9 +13,10 @@ constexpr int kMaxBits = 21;
 constexpr int kMaxLevels = kMaxBits + 1;
 constexpr int kMaxPasses = 8;           // 8-bit radix digits of a 63-bit key
 
-// Radix sort tile: 256 threads x 12 keys.
+// Radix sort tile: 256 threads x 16 keys (4096 keys: at 2^20 keys every
+// resident block sorts exactly one tile per pass).
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 12;
+constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;
 
 // Tree build tile: 256 threads x 4 positions.
