@@ -13,11 +13,14 @@ constexpr int kMaxBits = 21;
 constexpr int kMaxLevels = kMaxBits + 1;
 constexpr int kMaxPasses = 8;           // 8-bit radix digits of a 63-bit key
 
-// Radix sort tile: 256 threads x 16 keys (4096 keys: at 2^20 keys every
-// resident block sorts exactly one tile per pass).
+// Radix sort tiles: 256 threads x 16 keys (4096) once there are more
+// 3072-key tiles than resident blocks (at 2^20 keys every block then sorts
+// exactly one tile per pass), 256 x 12 keys below that (shorter tiles when
+// each block has one anyway).  Look-back slots are sized for the smaller.
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 16;
-constexpr int kSortTile = kSortThreads * kSortItems;
+constexpr int kSortItemsSmall = 12;
+constexpr int kSortItemsLarge = 16;
+constexpr int kSortTile = kSortThreads * kSortItemsSmall;
 
 // Tree build tile: 256 threads x 4 positions.
 constexpr int kBuildThreads = 256;

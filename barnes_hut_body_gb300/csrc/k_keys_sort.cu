@@ -300,11 +300,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned b
 
 constexpr unsigned kTmaWaitLimit = 1u << 26;   // polls; a bulk copy takes microseconds
 
+template <int ITEMS>
 struct SortSmem {
   // Two input stages (keys, then indices).  A stage's data is read into
   // registers, then the stage is reused to stage the scatter.
-  alignas(128) unsigned long long k[2][kSortTile];
-  alignas(128) unsigned int v[2][kSortTile];
+  alignas(128) unsigned long long k[2][kSortThreads * ITEMS];
+  alignas(128) unsigned int v[2][kSortThreads * ITEMS];
   unsigned int whist[kSortThreads / 32][256];
   unsigned int dig_excl[256];
   unsigned int glob[256];
@@ -317,7 +318,7 @@ struct SortSmem {
 // Persistent pass: each block takes tile tickets in order, one ahead, and
 // prefetches the next tile with TMA bulk copies while it ranks, looks back
 // and scatters the current one.
-template <bool kFirst>
+template <bool kFirst, int ITEMS>
 __global__ void __launch_bounds__(kSortThreads, 2)
 sort_pass_kernel(const unsigned long long *__restrict__ kin,
                  const unsigned int *__restrict__ vin,
@@ -328,7 +329,8 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
                  unsigned int tag_base, DevCtrl *ctrl,
                  unsigned int spin_limit) {
   extern __shared__ __align__(128) unsigned char sort_smem_raw[];
-  SortSmem &S = *reinterpret_cast<SortSmem *>(sort_smem_raw);
+  constexpr int kTile = kSortThreads * ITEMS;
+  SortSmem<ITEMS> &S = *reinterpret_cast<SortSmem<ITEMS> *>(sort_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const unsigned long long tag =
       (unsigned long long)(tag_base + ctrl->keep.epoch * 16u) << 32;
@@ -336,8 +338,8 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
   auto issue = [&](int b, long long t) {
     // keys (and indices) of tile t into stage b; sizes rounded up to 16
     // bytes (the buffers are padded past n)
-    const long long base = t * kSortTile;
-    const long long cnt = n - base < kSortTile ? n - base : kSortTile;
+    const long long base = t * kTile;
+    const long long cnt = n - base < kTile ? n - base : kTile;
     const unsigned kb = (unsigned)((cnt * 8 + 15) & ~15LL);
     const unsigned vb = kFirst ? 0u : (unsigned)((cnt * 4 + 15) & ~15LL);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -381,14 +383,14 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
       }
       parity[b] ^= 1u;
     }
-    const long long base = tile * kSortTile;
-    const int wbase = w * (kSortItems * 32);
+    const long long base = tile * kTile;
+    const int wbase = w * (ITEMS * 32);
 
-    unsigned long long key[kSortItems];
-    unsigned int val[kSortItems];
-    unsigned int rnk[kSortItems];
+    unsigned long long key[ITEMS];
+    unsigned int val[ITEMS];
+    unsigned int rnk[ITEMS];
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       const int j = wbase + i * 32 + lane;
       const bool valid = base + j < n;
       key[i] = valid ? S.k[b][j] : ~0ull;
@@ -397,7 +399,7 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
     }
     __syncthreads();                       // whist zeroed
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       unsigned d = (unsigned)(key[i] >> shift) & 255u;
       unsigned peers = 0xffffffffu;
 #pragma unroll
@@ -438,7 +440,7 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
     __syncthreads();
     // scatter into the stage in digit order
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       unsigned dd = (unsigned)(key[i] >> shift) & 255u;
       unsigned pos = S.dig_excl[dd] + S.whist[w][dd] + rnk[i];
       S.k[b][pos] = key[i];
@@ -478,7 +480,7 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
     S.glob[d] = S.gofs[d] + excl;
     __syncthreads();
     // write out: consecutive slots of one digit go to consecutive addresses
-    const long long nvalid = n - base < kSortTile ? n - base : kSortTile;
+    const long long nvalid = n - base < kTile ? n - base : kTile;
     for (int j = tid; j < nvalid; j += kSortThreads) {
       unsigned long long k = S.k[b][j];
       unsigned dd = (unsigned)(k >> shift) & 255u;
@@ -537,21 +539,20 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
   return cudaGetLastError();
 }
 
-cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
-                        int which, unsigned spin_limit, int *final_buf,
-                        cudaStream_t s) {
+template <int ITEMS>
+void sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
+                 unsigned spin_limit, int *final_buf, cudaStream_t s) {
   static bool attr = false;
-  const size_t smem = sizeof(SortSmem);
+  const size_t smem = sizeof(SortSmem<ITEMS>);
   if (!attr) {
-    cudaFuncSetAttribute(sort_pass_kernel<true>,
+    cudaFuncSetAttribute(sort_pass_kernel<true, ITEMS>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(sort_pass_kernel<false>,
+    cudaFuncSetAttribute(sort_pass_kernel<false, ITEMS>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  const int passes = (3 * bits + 7) / 8;
-  const long long tiles = (n + kSortTile - 1) / kSortTile;
-  if (tiles > b.cap_tiles) return cudaErrorInvalidValue;
+  constexpr long long kTile = (long long)kSortThreads * ITEMS;
+  const long long tiles = (n + kTile - 1) / kTile;
   long long grid = (long long)sm_count() * 2;
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
@@ -561,16 +562,29 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
     unsigned *ctr = &ctrl->step.tile_ctr[which][p];
     unsigned tag = (unsigned)(which * 8 + p);
     if (p == 0)
-      sort_pass_kernel<true><<<(unsigned)grid, kSortThreads, smem, s>>>(
+      sort_pass_kernel<true, ITEMS><<<(unsigned)grid, kSortThreads, smem, s>>>(
           b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
     else
-      sort_pass_kernel<false><<<(unsigned)grid, kSortThreads, smem, s>>>(
+      sort_pass_kernel<false, ITEMS><<<(unsigned)grid, kSortThreads, smem, s>>>(
           b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
     cur ^= 1;
   }
   *final_buf = cur;
+}
+
+cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
+                        int which, unsigned spin_limit, int *final_buf,
+                        cudaStream_t s) {
+  const int passes = (3 * bits + 7) / 8;
+  const long long tiles_small = (n + kSortTile - 1) / kSortTile;
+  if (tiles_small > b.cap_tiles) return cudaErrorInvalidValue;
+  // 4096-key tiles once 3072-key tiles outnumber the resident blocks
+  if (tiles_small > 2LL * sm_count())
+    sort_passes<kSortItemsLarge>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
+  else
+    sort_passes<kSortItemsSmall>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
   return cudaGetLastError();
 }
 
