@@ -190,10 +190,14 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
       ghi_z = fmaxf(ghi_z, __shfl_xor_sync(kFull, ghi_z, o));
       ghq = fmaxf(ghq, __shfl_xor_sync(kFull, ghq, o));
     }
-    // a group is spread out when its box is wider than its largest search
-    // radius; then the per-particle node test pays for itself
+    // a group is spread out when its box is wider than half its largest
+    // search radius; then the per-particle node test pays for itself.  (At
+    // the full radius a group in the sparse outskirts whose box is just
+    // under its one huge sphere -- h ~ 0.46 in a 2^18 Plummer sphere -- opened
+    // a large part of the halo and walked 1.2M pair tests on one warp,
+    // setting the time of the whole kernel.)
     const float ext = fmaxf(fmaxf(ghi_x - glo_x, ghi_y - glo_y), ghi_z - glo_z);
-    const bool spread = ext > kappa * ghq;
+    const bool spread = ext > 0.5f * kappa * ghq;
     unsigned cnt = 0, tests = 0;
     unsigned long long base = 0;
     const unsigned dst = valid ? perm[qi] : 0u;
