@@ -26,7 +26,7 @@ struct bh_ctx {
   int device = 0;
   int num_sms = 1;
   float theta = 0.5f, G = 1.f, eps = 0.f;
-  int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 64;
+  int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 0;
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
   int pipeline = 1;
   int order = BH_ORDER_RADIX;
@@ -325,12 +325,15 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   a.G = c->G;
   a.self_mode = self ? 1 : 0;
   a.opening = c->opening;
-  a.group = c->group;
+  // groups of 64, or of 32 when the targets fill fewer groups of 64 than the
+  // walk has warps taking groups (16 per SM): then the smaller groups walk in
+  // parallel what the larger ones would walk one after the other
+  a.group = c->group ? c->group : ((M + 63) / 64 < 16LL * c->num_sms ? 32 : 64);
   a.num_sms = c->num_sms;
   a.pipelined = c->pipeline;
   {
     // the walk order's groups, split into `shards` contiguous ranges
-    const long long gs = c->estimator == BH_EST_STOCHASTIC ? 32 : c->group;
+    const long long gs = c->estimator == BH_EST_STOCHASTIC ? 32 : a.group;
     const long long ng = (M + gs - 1) / gs;
     a.g_begin = ng * c->shard / c->shards;
     a.g_end = ng * (c->shard + 1) / c->shards;
@@ -461,7 +464,7 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       c->use_graph = v ? 1 : 0;
       return BH_OK;
     case BH_OPT_GROUP:
-      if (v != 32 && v != 64) return fail(c, BH_EINVAL, "group must be 32 or 64");
+      if (v != 0 && v != 32 && v != 64) return fail(c, BH_EINVAL, "group must be 0, 32 or 64");
       c->group = (int)v;
       return BH_OK;
     case BH_OPT_ESTIMATOR:

@@ -282,10 +282,24 @@ def stage_bytes(n: int, m: int, nodes: int, self_mode: bool, order: str = "radix
     return b
 
 
+def walk_group(m: int) -> int:
+    """The library's default group size for m targets (BH_OPT_GROUP 0): 64,
+    or 32 when m fills fewer groups of 64 than 16 per SM."""
+    sms = 152
+    try:
+        import torch
+        if torch.cuda.is_available():
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 32 if (m + 63) // 64 < 16 * sms else 64
+
+
 def workload_config(name, src, tgt, theta, eps, order="radix", fused=False):
+    m = int(src.shape[0] if tgt is None else tgt.shape[0])
     return {"workload": name, "n_sources": int(src.shape[0]),
-            "n_targets": int(src.shape[0] if tgt is None else tgt.shape[0]),
-            "theta": theta, "eps": eps, "opening": "warp vote, groups of 64",
+            "n_targets": m,
+            "theta": theta, "eps": eps, "opening": f"warp vote, groups of {walk_group(m)}",
             "walk": "fused" if fused else "producer/consumer warp pairs",
             "leaf_cap": 16, "key_bits": 63, "order": order,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}

@@ -59,7 +59,11 @@ typedef struct bh_ctx bh_ctx;
                                    cell is subdivided while it holds > B     */
 #define BH_OPT_OPENING       3  /* group opening rule, see BH_OPEN_*         */
 #define BH_OPT_TIMING        4  /* 1: record per-stage CUDA events (default 0) */
-#define BH_OPT_GROUP         5  /* targets per warp group: 32 or 64 (default 64) */
+#define BH_OPT_GROUP         5  /* targets per warp group: 32, 64, or 0 (default):
+                                   64, or 32 when the targets fill fewer groups
+                                   of 64 than 16 per SM (below ~155k targets
+                                   on 152 SMs) -- the opening vote is then
+                                   taken over 32 targets                    */
 #define BH_OPT_GRAPH         6  /* 1 (default): a call that repeats the previous
                                    one exactly (pointers, sizes, parameters,
                                    options) is captured once as a CUDA graph

@@ -102,7 +102,7 @@ def test_unsorted_targets_and_far_targets(B):
     g = W.rng(10)
     tgt = np.zeros((777, 4), np.float32)
     tgt[:, :3] = g.uniform(-2.0, 3.0, size=(777, 3))
-    _, got, rc = H.gpu_bh(src, tgt, theta=0.5, eps=1e-3)
+    _, got, rc = H.gpu_bh(src, tgt, theta=0.5, eps=1e-3, group=64)
     assert rc == 0
     o = O.OracleBH(src, theta=0.5, eps=1e-3, leaf_cap=16)
     ref, rows, _, mag = o.bh_group(tgt, group=64, mode=0, with_abs=True)

@@ -119,17 +119,37 @@ def test_walk_matches_oracle_group_walk(name, theta, group, opening, pipeline):
 def test_pipelined_walk_is_the_fused_walk_bit_for_bit(name, opening):
     # same list order, same pairing, same arithmetic: identical results
     src = SETS[name]
-    bh0, a, rc0 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=0)
-    bh1, b, rc1 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=1)
+    bh0, a, rc0 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=0, group=64)
+    bh1, b, rc1 = H.gpu_bh(src, theta=0.5, eps=1e-3, opening=opening, pipeline=1, group=64)
     assert rc0 == 0 and rc1 == 0
     np.testing.assert_array_equal(a, b)
     import barnes_hut_body_gb300 as B
     assert B.bh_get_counters(bh0.ctx) == B.bh_get_counters(bh1.ctx)
     tgt = W.query_grid(src, side=17)
-    _, a, rc0 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=0)
-    _, b, rc1 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=1)
+    _, a, rc0 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=0, group=64)
+    _, b, rc1 = H.gpu_bh(src, tgt, theta=0.5, eps=0.0, opening=opening, pipeline=1, group=64)
     assert rc0 == 0 and rc1 == 0
     np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["uniform4096", "plummer_2e15", "ragged_12345"])
+def test_automatic_group_size(name):
+    # with the default group option, targets that fill fewer groups of 64
+    # than the walk has warps (16 per SM) are walked in groups of 32: the
+    # vote over 32 targets, exactly the oracle's group walk of 32
+    import barnes_hut_body_gb300 as B
+    import torch
+    src = SETS[name]
+    n = src.shape[0]
+    bh, got, rc = H.gpu_bh(src, theta=0.5, eps=1e-3)
+    assert rc == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    group = 32 if (n + 63) // 64 < 16 * sms else 64
+    assert B.bh_get_counters(bh.ctx)[1] == (n + group - 1) // group
+    o = O.OracleBH(src, theta=0.5, eps=1e-3, leaf_cap=16)
+    ref, rows, _, mag = o.bh_group(group=group, mode=0, with_abs=True)
+    H.assert_walk_close(got[rows], ref, f"{name} auto group {group}", mag)
+    bh.close()
 
 
 def test_theta_zero_is_the_direct_sum():
@@ -144,7 +164,7 @@ def test_theta_zero_is_the_direct_sum():
 def test_source_target_walk(opening):
     src = W.ellipsoid_surfaces(1 << 15, seed=2)
     tgt = W.query_grid(src, side=30)
-    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, G=1.0, eps=1e-4, opening=opening)
+    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, G=1.0, eps=1e-4, opening=opening, group=64)
     assert rc == 0
     import barnes_hut_body_gb300 as B
     tperm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, tgt.shape[0])
@@ -159,7 +179,7 @@ def test_source_target_walk(opening):
 
 def test_eps_zero():
     src = W.uniform_cube(4096, seed=12)
-    _, got, rc = H.gpu_bh(src, theta=0.5, eps=0.0)
+    _, got, rc = H.gpu_bh(src, theta=0.5, eps=0.0, group=64)
     assert rc == 0
     o = O.OracleBH(src, theta=0.5, eps=0.0, leaf_cap=16)
     ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
@@ -172,7 +192,7 @@ def test_eps_zero():
 @pytest.mark.parametrize("leaf_cap", [1, 64])
 def test_walk_other_leaf_caps(leaf_cap):
     src = SETS["plummer_2e15"]
-    _, got, rc = H.gpu_bh(src, theta=0.5, leaf_cap=leaf_cap)
+    _, got, rc = H.gpu_bh(src, theta=0.5, leaf_cap=leaf_cap, group=64)
     assert rc == 0
     o = O.OracleBH(src, theta=0.5, leaf_cap=leaf_cap)
     ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
@@ -181,7 +201,7 @@ def test_walk_other_leaf_caps(leaf_cap):
 
 def test_gravity_constant_and_thirty_bit_keys():
     src = SETS["uniform4096"]
-    _, got, rc = H.gpu_bh(src, theta=0.6, G=2.5, eps=2e-3, key_bits=10)
+    _, got, rc = H.gpu_bh(src, theta=0.6, G=2.5, eps=2e-3, key_bits=10, group=64)
     assert rc == 0
     o = O.OracleBH(src, theta=0.6, G=2.5, eps=2e-3, bits=10, leaf_cap=16)
     ref, rows, _, mag = o.bh_group(group=64, mode=0, with_abs=True)
