@@ -30,6 +30,7 @@ struct bh_ctx {
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
   int pipeline = 1;
   int order = BH_ORDER_RADIX;
+  int order_factor = 2;             // insertion-tree pool: nodes per row
   int shards = 1, shard = 0;        // walk only shard `shard` of `shards`
   unsigned long long seed = 0;
   int *strata = nullptr;
@@ -71,7 +72,7 @@ struct bh_ctx {
   struct Key {
     const void *pm, *tg;
     void *out;
-    long long n, m, cap_n, cap_m;
+    long long n, m, cap_n, cap_m, cap_order;   // capacities: buffers reallocated
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
@@ -151,12 +152,15 @@ void free_order(bh_ctx *c) {
   b.cap_nodes = 0;
 }
 
-// The insertion tree's pool: 2 rows + 64 nodes.  A node is a Morton (or
-// index) digit prefix that two or more rows share; the measured workloads
-// need 0.25-0.72 nodes per row, but rows that agree on long prefixes (near
-// duplicates) can need more, which the build reports as BH_ETREE_OVERFLOW.
+// The insertion tree's pool: order_factor x rows + 64 nodes (factor 2 at
+// first).  A node is a Morton (or index) digit prefix that two or more rows
+// share; the measured workloads need 0.25-0.72 nodes per row, but rows that
+// agree on long prefixes (near duplicates) can need more, which the build
+// reports as BH_ETREE_OVERFLOW; bh_sync_status then raises the factor 4x for
+// the next call, up to 32 -- enough for any input: with 31 digit levels the
+// tree has at most 1 + 31 (rows - 1) nodes.
 int ensure_order(bh_ctx *c, long long rows) {
-  const long long want = 2 * rows + 64;
+  const long long want = (long long)c->order_factor * rows + 64;
   if (want <= c->order_bufs.cap_nodes) return BH_OK;
   cudaDeviceSynchronize();
   free_order(c);
@@ -559,6 +563,7 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   memset(&key, 0, sizeof(key));
   key.pm = pm; key.tg = tg; key.out = out; key.n = N; key.m = M;
   key.cap_n = c->cap_n; key.cap_m = c->cap_m;
+  key.cap_order = c->order_bufs.cap_nodes;
   key.theta = c->theta; key.G = c->G; key.eps = c->eps;
   key.bits = c->bits; key.leaf_cap = c->leaf_cap; key.opening = c->opening;
   key.group = c->group; key.spin = c->spin_limit;
@@ -627,6 +632,13 @@ int bh_sync_status(bh_ctx *c, void *stream) {
   if (e != cudaSuccess) return cuda_fail(c, e, "status read");
   if (err) {
     cudaMemset(&c->ctrl->keep.err, 0, sizeof(unsigned));
+    // a row left out of the insertion tree: the next call gets a larger pool
+    unsigned order_fail = 0;
+    if (err == BH_ETREE_OVERFLOW && c->order == BH_ORDER_TREE &&
+        cudaMemcpy(&order_fail, &c->ctrl->step.order_fail, sizeof(unsigned),
+                   cudaMemcpyDeviceToHost) == cudaSuccess &&
+        order_fail && c->order_factor < 32)
+      c->order_factor = c->order_factor * 4 < 32 ? c->order_factor * 4 : 32;
     const char *what = err == BH_EINVAL ? "non-finite input"
                        : err == BH_ETIMEOUT ? "a device wait timed out"
                        : err == BH_ETREE_OVERFLOW ? "node pool or walk stack overflow"

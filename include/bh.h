@@ -107,8 +107,11 @@ typedef struct bh_ctx bh_ctx;
  *   (key, index) order.  Its node pool (80 bytes x (2 rows + 64), allocated
  *   at the first call that uses it) is enough for every measured workload
  *   (0.25-0.72 nodes per row); rows sharing very long digit prefixes can
- *   exhaust it, which bh_sync_status reports as BH_ETREE_OVERFLOW.  Measured
- *   slower than BH_ORDER_RADIX on GB300; kept as the page's method.
+ *   exhaust it, which bh_sync_status reports as BH_ETREE_OVERFLOW; the next
+ *   call then gets a 4x larger pool (at most 32 nodes per row, which always
+ *   suffices: the tree has at most 1 + 31 (rows - 1) nodes), so repeating
+ *   the call succeeds.  Measured slower than BH_ORDER_RADIX on GB300; kept
+ *   as the page's method.
  */
 /*
  * Shards.  The walk visits the targets in Morton order, in groups (of

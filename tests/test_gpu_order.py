@@ -106,12 +106,25 @@ def test_tree_order_neighbour_search(B):
 
 def test_tree_order_pool_overflow_is_reported_and_recovers(B):
     # 2000 pairs need ~17 trie nodes per pair, far beyond the pool of
-    # 2 x rows + 64 nodes: the build flags BH_ETREE_OVERFLOW, later stages
-    # run on the identity order, and the next call is exact again
+    # 2 x rows + 64 nodes: the build flags BH_ETREE_OVERFLOW and later stages
+    # run on the identity order; the status read grows the pool 4x, so the
+    # same call repeated is exact (the radix path's result, bit for bit);
+    # and another input is exact too
     src = _near_duplicate_pairs(2000, seed=5)
+    for graph in (0, 1):
+        bh = B.BarnesHut(theta=0.5, eps=1e-3, order=B.BH_ORDER_TREE, graph=graph)
+        d = H.to_dev(src)
+        bh.compute(d)
+        assert bh.status() == B.BH_ETREE_OVERFLOW
+        again = [bh.compute(d).cpu().numpy().astype(np.float64) for _ in range(3)]
+        assert bh.status() == 0
+        _, ref_pairs, rc = H.gpu_bh(src, eps=1e-3)
+        assert rc == 0
+        for a in again:
+            np.testing.assert_array_equal(a, ref_pairs)
+        bh.close()
     bh = B.BarnesHut(theta=0.5, eps=1e-3, order=B.BH_ORDER_TREE, graph=0)
-    d = H.to_dev(src)
-    bh.compute(d)
+    bh.compute(H.to_dev(src))
     assert bh.status() == B.BH_ETREE_OVERFLOW
     ok = H.to_dev(SETS["uniform4096"])
     got = bh.compute(ok).cpu().numpy().astype(np.float64)
