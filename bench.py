@@ -43,15 +43,12 @@ FLOPS_PER_TERM = 20
 # (FMA) x 2070 MHz (maximum SM clock).
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
-# Our kernels per step with 63-bit keys: per particle set bbox, keys and the
-# order (8 radix passes + gather, or the tree order's init, insert, node
-# count, count and place kernels); then build count/scan/write, centre of
-# mass and walk.
-KERNELS_PER_STEP = {21: 16, 10: 12}
-
-
 def kernels_per_step(order: str, self_mode: bool) -> int:
-    per_set = 2 + (9 if order == "radix" else 5)
+    """Our kernels per step with 63-bit keys: per particle set bbox, keys and
+    the order (8 radix passes + gather, or the tree order's histogram, top
+    levels, insert, node count, count and place kernels); then build
+    count/scan/write, centre of mass and walk."""
+    per_set = 2 + (9 if order == "radix" else 6)
     return per_set * (1 if self_mode else 2) + 5
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
