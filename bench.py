@@ -52,7 +52,7 @@ def kernels_per_step(order: str, self_mode: bool) -> int:
     return per_set * (1 if self_mode else 2) + 5
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = None   # the walk kernel changed since the last capture
+WALK_TRAFFIC_BYTES = 29.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
