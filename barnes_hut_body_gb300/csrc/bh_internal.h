@@ -4,9 +4,40 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "bh.h"
 
 namespace bh {
+
+// Host-side memo of a per-device launch property (SM count, resident blocks
+// per SM, a kernel's shared-memory opt-in).  Such properties belong to one
+// device, and one process may drive several devices through separate
+// contexts, so each device (the current one at the call) gets its own slot;
+// `make` runs once per device and must return a nonzero value.
+constexpr int kMaxDevices = 64;
+template <class F>
+inline int per_device(std::atomic<int> (&memo)[kMaxDevices], F make) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return make();
+  int v = memo[d].load(std::memory_order_relaxed);
+  if (v == 0) {
+    v = make();
+    memo[d].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+// Number of SMs of the current device (at least 1).
+inline int sm_count() {
+  static std::atomic<int> memo[kMaxDevices];
+  return per_device(memo, [] {
+    int dev = 0, c = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    return c > 0 ? c : 1;
+  });
+}
 
 // Octree levels 0..21 (21 bits per axis of a 63-bit Morton key).
 constexpr int kMaxBits = 21;

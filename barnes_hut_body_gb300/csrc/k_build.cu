@@ -406,17 +406,6 @@ com_kernel(const float4 *__restrict__ spm, const unsigned long long *skeys,
   }
 }
 
-int sm_count() {
-  static int c = 0;
-  if (c == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    if (c <= 0) c = 1;
-  }
-  return c;
-}
-
 }  // namespace
 
 cudaError_t launch_build(const unsigned long long *skeys, long long n, int bits,

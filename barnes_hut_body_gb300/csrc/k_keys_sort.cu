@@ -505,17 +505,6 @@ __global__ void gather_kernel(const float4 *__restrict__ in,
   }
 }
 
-int sm_count() {
-  static int c = 0;
-  if (c == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    if (c <= 0) c = 1;
-  }
-  return c;
-}
-
 }  // namespace
 
 cudaError_t launch_bbox(const float4 *pm, long long n, float4 *partials,
@@ -542,15 +531,15 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
 template <int ITEMS>
 void sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
                  unsigned spin_limit, int *final_buf, cudaStream_t s) {
-  static bool attr = false;
+  static std::atomic<int> attr[kMaxDevices];
   const size_t smem = sizeof(SortSmem<ITEMS>);
-  if (!attr) {
+  per_device(attr, [smem] {
     cudaFuncSetAttribute(sort_pass_kernel<true, ITEMS>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(sort_pass_kernel<false, ITEMS>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
-  }
+    return 1;
+  });
   constexpr long long kTile = (long long)kSortThreads * ITEMS;
   const long long tiles = (n + kTile - 1) / kTile;
   long long grid = (long long)sm_count() * 2;

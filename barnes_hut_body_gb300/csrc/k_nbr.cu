@@ -402,12 +402,13 @@ scan_apply(const unsigned int *__restrict__ x, long long n,
 
 template <bool kSym, bool kFill>
 cudaError_t launch_walk_t(const NbArgs &a, DevCtrl *ctrl, cudaStream_t s) {
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nb_walk_kernel<kSym, kFill>,
+  static std::atomic<int> memo[kMaxDevices];
+  const int per_sm = per_device(memo, [] {
+    int b = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, nb_walk_kernel<kSym, kFill>,
                                                   kNbThreads, 0);
-    if (per_sm < 1) per_sm = 1;
-  }
+    return b > 0 ? b : 1;
+  });
   const long long ngroups = (a.n + 31) / 32;
   long long blocks = (ngroups + kNbWarps - 1) / kNbWarps;
   const long long cap = (long long)a.num_sms * per_sm;

@@ -333,17 +333,18 @@ cudaError_t launch_sbh(const SbhArgs &a, int *strata, int strata_cap,
   strata_kernel<<<1, 1024, 0, s>>>(a.rec, a.nodes, a.strata_level, strata_cap, strata, ctrl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  static int per_sm[2] = {0, 0};
-  const int k = a.self_mode ? 1 : 0;
-  if (per_sm[k] == 0) {
-    if (a.self_mode)
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[k], sbh_kernel<true>, kSbhThreads, 0);
+  static std::atomic<int> memo[2][kMaxDevices];
+  const bool self = a.self_mode != 0;
+  const int per_sm = per_device(memo[self ? 1 : 0], [self] {
+    int b = 0;
+    if (self)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, sbh_kernel<true>, kSbhThreads, 0);
     else
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[k], sbh_kernel<false>, kSbhThreads, 0);
-    if (per_sm[k] < 1) per_sm[k] = 1;
-  }
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, sbh_kernel<false>, kSbhThreads, 0);
+    return b > 0 ? b : 1;
+  });
   const long long ngroups = a.g_end - a.g_begin;
-  long long blocks = (long long)a.num_sms * per_sm[k];
+  long long blocks = (long long)a.num_sms * per_sm;
   const long long need = (ngroups + kSbhThreads / 32 - 1) / (kSbhThreads / 32);
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;

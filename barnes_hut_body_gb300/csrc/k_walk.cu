@@ -956,12 +956,13 @@ count_kernel(const NodeRec *__restrict__ rec, const float4 *__restrict__ tpos,
 
 template <int T, bool kVote, bool kEps0, bool kSelf>
 cudaError_t launch_ws(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static std::atomic<int> memo[kMaxDevices];
+  const int per_sm = per_device(memo, [] {
+    int b = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, walk_ws_kernel<T, kVote, kEps0, kSelf>, kWsThreads, 0);
-    if (per_sm < 1) per_sm = 1;
-  }
+        &b, walk_ws_kernel<T, kVote, kEps0, kSelf>, kWsThreads, 0);
+    return b > 0 ? b : 1;
+  });
   const long long ngroups = a.g_end - a.g_begin;
   long long blocks = (long long)a.num_sms * per_sm;
   const long long need = (ngroups + kWsPairs - 1) / kWsPairs;
@@ -980,12 +981,13 @@ cudaError_t launch_one(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
   } else {
     if (a.pipelined) return launch_ws<T, kVote, kEps0, kSelf>(a, ctrl, s);
   }
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static std::atomic<int> memo[kMaxDevices];
+  const int per_sm = per_device(memo, [] {
+    int b = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, walk_kernel<T, kVote, kEps0, kSelf>, kWalkThreads, 0);
-    if (per_sm < 1) per_sm = 1;
-  }
+        &b, walk_kernel<T, kVote, kEps0, kSelf>, kWalkThreads, 0);
+    return b > 0 ? b : 1;
+  });
   const long long ngroups = a.g_end - a.g_begin;
   long long blocks = (long long)a.num_sms * per_sm;
   long long need = (ngroups + kWalkWarps - 1) / kWalkWarps;
