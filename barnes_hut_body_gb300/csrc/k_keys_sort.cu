@@ -298,6 +298,27 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned b
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// Rank of this lane's digit d among the warp's keys of the same digit so far:
+// lanes holding d (found with eight ballots) count before it in lane order,
+// on top of the warp's running count `row[d]`, which the lowest such lane
+// then advances.  Keys ranked one item after another keep their order, so
+// the sort is stable.
+__device__ __forceinline__ unsigned warp_rank(unsigned d, unsigned *row, unsigned lt) {
+  unsigned peers = 0xffffffffu;
+#pragma unroll
+  for (int bt = 0; bt < 8; ++bt) {
+    unsigned bit = (d >> bt) & 1u;
+    unsigned bal = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? bal : ~bal;
+  }
+  const unsigned before = row[d];
+  const unsigned r = before + __popc(peers & lt);
+  __syncwarp();
+  if ((peers & lt) == 0u) row[d] = before + __popc(peers);
+  __syncwarp();
+  return r;
+}
+
 constexpr unsigned kTmaWaitLimit = 1u << 26;   // polls; a bulk copy takes microseconds
 
 template <int ITEMS>
@@ -399,21 +420,8 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
     }
     __syncthreads();                       // whist zeroed
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      unsigned d = (unsigned)(key[i] >> shift) & 255u;
-      unsigned peers = 0xffffffffu;
-#pragma unroll
-      for (int bt = 0; bt < 8; ++bt) {
-        unsigned bit = (d >> bt) & 1u;
-        unsigned bal = __ballot_sync(0xffffffffu, bit);
-        peers &= bit ? bal : ~bal;
-      }
-      unsigned before = S.whist[w][d];
-      rnk[i] = before + __popc(peers & lt);
-      __syncwarp();
-      if ((peers & lt) == 0u) S.whist[w][d] = before + __popc(peers);
-      __syncwarp();
-    }
+    for (int i = 0; i < ITEMS; ++i)
+      rnk[i] = warp_rank((unsigned)(key[i] >> shift) & 255u, S.whist[w], lt);
     __syncthreads();
     // per digit: offsets of the warps within the tile, and the tile's count
     const unsigned d = tid;
@@ -494,6 +502,105 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Short arrays: the whole sort in one block.  At a few thousand keys each
+// tile pass above is one tile and costs its launch and ramp (~8 us, 8 passes
+// ~64 us at 4096 keys); here every digit pass ranks, scans and scatters in
+// shared memory, one launch for all of them.  Same ranking (warp_rank, keys
+// handled in index order), so the same stable permutation.
+// ---------------------------------------------------------------------------
+constexpr int kSmallSortThreads = 1024;
+constexpr int kSmallSortItems = 4;
+constexpr int kSmallSortWarps = kSmallSortThreads / 32;
+constexpr int kSmallSortN = kSmallSortThreads * kSmallSortItems;   // 4096 keys
+constexpr int kSmallRow = 257;   // padded warp-count rows: the per-digit scan
+                                 // reads one column without bank conflicts
+
+struct SmallSortSmem {
+  alignas(16) unsigned long long k[2][kSmallSortN];
+  alignas(16) unsigned int v[2][kSmallSortN];
+  unsigned int whist[kSmallSortWarps * kSmallRow];
+  unsigned int dig[256];
+};
+
+__global__ void __launch_bounds__(kSmallSortThreads, 1)
+sort_small_kernel(const unsigned long long *__restrict__ kin, long long n, int passes,
+                  unsigned long long *__restrict__ kout, unsigned int *__restrict__ vout) {
+  extern __shared__ __align__(128) unsigned char small_sort_raw[];
+  SmallSortSmem &S = *reinterpret_cast<SmallSortSmem *>(small_sort_raw);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int wbase = w * (kSmallSortItems * 32);
+  // padding keys (all ones, larger than any 63-bit key) sort after the real ones
+  for (int j = tid; j < kSmallSortN; j += kSmallSortThreads) {
+    S.k[0][j] = j < n ? kin[j] : ~0ull;
+    S.v[0][j] = (unsigned)j;
+  }
+  int cur = 0;
+  for (int p = 0; p < passes; ++p) {
+    const int shift = 8 * p;
+    for (int k = tid; k < kSmallSortWarps * kSmallRow; k += kSmallSortThreads) S.whist[k] = 0u;
+    __syncthreads();                       // counts zeroed (and the first stage loaded)
+    unsigned long long key[kSmallSortItems];
+    unsigned int val[kSmallSortItems], rnk[kSmallSortItems];
+#pragma unroll
+    for (int i = 0; i < kSmallSortItems; ++i) {
+      const int j = wbase + i * 32 + lane;
+      key[i] = S.k[cur][j];
+      val[i] = S.v[cur][j];
+    }
+#pragma unroll
+    for (int i = 0; i < kSmallSortItems; ++i)
+      rnk[i] = warp_rank((unsigned)(key[i] >> shift) & 255u, &S.whist[w * kSmallRow], lt);
+    __syncthreads();
+    // per digit, the offsets of the warps (lane = warp) and the digit total:
+    // warp w takes digits 8w .. 8w+7
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int d = w * 8 + q;
+      const unsigned c = S.whist[lane * kSmallRow + d];
+      unsigned x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      S.whist[lane * kSmallRow + d] = x - c;
+      if (lane == 31) S.dig[d] = x;
+    }
+    __syncthreads();
+    // start of each digit: exclusive scan of the 256 totals (8 per lane)
+    if (w == 0) {
+      unsigned t[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { t[q] = S.dig[lane * 8 + q]; sum += t[q]; }
+      unsigned x = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      unsigned run = x - sum;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { S.dig[lane * 8 + q] = run; run += t[q]; }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kSmallSortItems; ++i) {
+      const unsigned d = (unsigned)(key[i] >> shift) & 255u;
+      const unsigned pos = S.dig[d] + S.whist[w * kSmallRow + d] + rnk[i];
+      S.k[cur ^ 1][pos] = key[i];
+      S.v[cur ^ 1][pos] = val[i];
+    }
+    cur ^= 1;
+    __syncthreads();                       // counts read by every warp's scatter
+  }
+  for (int j = tid; j < n; j += kSmallSortThreads) {
+    kout[j] = S.k[cur][j];
+    vout[j] = S.v[cur][j];
+  }
+}
+
 __global__ void gather_kernel(const float4 *__restrict__ in,
                               const unsigned int *__restrict__ perm,
                               long long n, float4 *__restrict__ out) {
@@ -567,6 +674,18 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
                         int which, unsigned spin_limit, int *final_buf,
                         cudaStream_t s) {
   const int passes = (3 * bits + 7) / 8;
+  if (n <= kSmallSortN) {
+    static std::atomic<int> attr[kMaxDevices];
+    per_device(attr, [] {
+      cudaFuncSetAttribute(sort_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(SmallSortSmem));
+      return 1;
+    });
+    sort_small_kernel<<<1, kSmallSortThreads, sizeof(SmallSortSmem), s>>>(
+        b.keys[0], n, passes, b.keys[1], b.idx[1]);
+    *final_buf = 1;
+    return cudaGetLastError();
+  }
   const long long tiles_small = (n + kSortTile - 1) / kSortTile;
   if (tiles_small > b.cap_tiles) return cudaErrorInvalidValue;
   // 4096-key tiles once 3072-key tiles outnumber the resident blocks

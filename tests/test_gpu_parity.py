@@ -47,6 +47,40 @@ def test_keys_and_permutation_bit_exact(name, bits):
     np.testing.assert_array_equal(keys, o.skeys)
 
 
+def _dup_points(n, seed):
+    d = W.uniform_cube(n, seed=seed)
+    d[n // 2:] = d[: n - n // 2]                  # every point twice (ties by index)
+    return d
+
+
+@pytest.mark.parametrize("n", [2, 3, 33, 1000, 4095, 4096, 4097, 8191])
+@pytest.mark.parametrize("bits", [21, 10])
+def test_permutation_bit_exact_around_the_one_block_sort(n, bits):
+    # up to 4096 keys the sort runs in one block (all digit passes in shared
+    # memory); above, one kernel per digit pass: both give the stable sort
+    src = _dup_points(n, seed=n)
+    bh, _, rc = H.gpu_bh(src, key_bits=bits)
+    assert rc == 0
+    keys, perm, _, _, cube = H.export_state(bh, n)
+    o = O.OracleBH(src, bits=bits, leaf_cap=16)
+    np.testing.assert_array_equal(cube, o.cube)
+    np.testing.assert_array_equal(perm, o.perm)
+    np.testing.assert_array_equal(keys, o.skeys)
+    bh.close()
+
+
+@pytest.mark.parametrize("m", [7, 4096, 4097])
+def test_target_permutation_around_the_one_block_sort(m):
+    import barnes_hut_body_gb300 as B
+    src = SETS["uniform4096"]
+    tgt = _dup_points(m, seed=m + 1)
+    bh, _, rc = H.gpu_bh(src, tgt)
+    assert rc == 0
+    ref = O.sort(O.keys(tgt, O.bbox(tgt), 21))
+    np.testing.assert_array_equal(B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, m), ref)
+    bh.close()
+
+
 @pytest.mark.parametrize("name", ["uniform4096", "plummer_2e15", "galaxy_2e16",
                                   "dups_5000", "ragged_12345"])
 @pytest.mark.parametrize("leaf_cap", [1, 8, 16, 64])
