@@ -27,13 +27,15 @@ BH_OPT_ESTIMATOR, BH_OPT_SEED, BH_OPT_SAMPLES, BH_OPT_STRATA_LEVEL = 7, 8, 9, 10
 BH_OPT_PIPELINE = 11
 BH_OPT_ORDER = 12
 BH_OPT_SHARDS, BH_OPT_SHARD = 13, 14
+BH_OPT_SCHEDULE = 15
 BH_ORDER_RADIX, BH_ORDER_TREE = 0, 1
 BH_EST_BARNES_HUT, BH_EST_STOCHASTIC = 0, 1
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
 BH_DBG_SPIN_LIMIT = 1
 BH_LF_ACC_VALID = 1
 (BH_EXPORT_CUBE, BH_EXPORT_KEYS, BH_EXPORT_PERM, BH_EXPORT_NODE_COUNT,
- BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM, BH_EXPORT_WALK_STATS) = range(1, 9)
+ BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM, BH_EXPORT_WALK_STATS,
+ BH_EXPORT_GROUP_COST, BH_EXPORT_GROUP_ORDER) = range(1, 11)
 STAGES = ("bbox", "keys", "sort", "reorder", "build", "com", "targets", "traverse")
 
 EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
@@ -286,7 +288,8 @@ def bh_debug_export(ctx, what: int, count: int = 0) -> np.ndarray:
         out = np.zeros(4, np.float32)
     elif what == BH_EXPORT_KEYS:
         out = np.zeros(count, np.uint64)
-    elif what in (BH_EXPORT_PERM, BH_EXPORT_TARGET_PERM):
+    elif what in (BH_EXPORT_PERM, BH_EXPORT_TARGET_PERM, BH_EXPORT_GROUP_COST,
+                  BH_EXPORT_GROUP_ORDER):
         out = np.zeros(count, np.uint32)
     elif what == BH_EXPORT_NODES:
         out = np.zeros((count, 6), np.int32)
@@ -326,7 +329,7 @@ _OPTION_KEYS = dict(key_bits=BH_OPT_KEY_BITS, leaf_cap=BH_OPT_LEAF_CAP,
                     graph=BH_OPT_GRAPH, estimator=BH_OPT_ESTIMATOR, seed=BH_OPT_SEED,
                     samples=BH_OPT_SAMPLES, strata_level=BH_OPT_STRATA_LEVEL,
                     pipeline=BH_OPT_PIPELINE, order=BH_OPT_ORDER, shards=BH_OPT_SHARDS,
-                    shard=BH_OPT_SHARD)
+                    shard=BH_OPT_SHARD, schedule=BH_OPT_SCHEDULE)
 
 
 class BarnesHut:

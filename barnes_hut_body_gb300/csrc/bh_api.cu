@@ -32,7 +32,16 @@ struct bh_ctx {
   int order = BH_ORDER_RADIX;
   int order_factor = 2;             // insertion-tree pool: nodes per row
   int shards = 1, shard = 0;        // walk only shard `shard` of `shards`
+  int schedule = 1;                 // BH_OPT_SCHEDULE
   unsigned long long seed = 0;
+  // group schedule: the last walk's terms per group, and the order built
+  // from them; `sched_groups` groups of `sched_gs` targets are valid
+  unsigned int *gcost = nullptr, *gorder = nullptr;
+  long long cap_groups = 0, sched_groups = -1;
+  int sched_gs = 0;
+  bool sched_now = false;           // this call walks in the scheduled order
+  long long last_groups = 0;        // groups of the last call's walk,
+  bool last_costs = false, last_ordered = false;   // costs recorded / order used
   int *strata = nullptr;
   int strata_cap = 0;
   // neighbour search scratch
@@ -72,11 +81,11 @@ struct bh_ctx {
   struct Key {
     const void *pm, *tg;
     void *out;
-    long long n, m, cap_n, cap_m, cap_order;   // capacities: buffers reallocated
+    long long n, m, cap_n, cap_m, cap_order, cap_groups;   // capacities: buffers reallocated
     float theta, G, eps;
     int bits, leaf_cap, opening, group;
     unsigned spin;
-    int estimator, samples, strata_level, pipeline, order, shards, shard;
+    int estimator, samples, strata_level, pipeline, order, shards, shard, schedule, sched;
     unsigned long long seed;
     bool operator==(const Key &o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
   };
@@ -249,6 +258,36 @@ int ensure_targets(bh_ctx *c, long long m) {
   return ensure_status(c, cap);
 }
 
+// Targets per walk group: the stochastic estimator's 32; else BH_OPT_GROUP,
+// or by default 64, or 32 when the targets fill fewer groups of 64 than the
+// walk has warps taking groups (16 per SM): then the smaller groups walk in
+// parallel what the larger ones would walk one after the other.
+long long walk_group_size(const bh_ctx *c, long long m) {
+  if (c->estimator == BH_EST_STOCHASTIC) return 32;
+  if (c->group) return c->group;
+  return (m + 63) / 64 < 16LL * c->num_sms ? 32 : 64;
+}
+
+// Per-group cost and order buffers for m targets (groups of >= 32).  A new
+// allocation holds no costs, so the schedule starts over.
+int ensure_sched(bh_ctx *c, long long m) {
+  const long long need = (m + 31) / 32;
+  if (need <= c->cap_groups) return BH_OK;
+  cudaDeviceSynchronize();
+  free_dev(c->gcost);
+  free_dev(c->gorder);
+  c->cap_groups = 0;
+  c->sched_groups = -1;
+  const long long cap = need + need / 8 + 64;
+  if (!alloc_dev(c->gcost, cap) || !alloc_dev(c->gorder, cap)) {
+    free_dev(c->gcost);
+    free_dev(c->gorder);
+    return fail(c, BH_ENOMEM, "group schedule buffers");
+  }
+  c->cap_groups = cap;
+  return BH_OK;
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 int check_rows(bh_ctx *c, const float *p, size_t rows, const char *name) {
@@ -329,19 +368,22 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   a.G = c->G;
   a.self_mode = self ? 1 : 0;
   a.opening = c->opening;
-  // groups of 64, or of 32 when the targets fill fewer groups of 64 than the
-  // walk has warps taking groups (16 per SM): then the smaller groups walk in
-  // parallel what the larger ones would walk one after the other
   a.group = c->group ? c->group : ((M + 63) / 64 < 16LL * c->num_sms ? 32 : 64);
   a.num_sms = c->num_sms;
   a.pipelined = c->pipeline;
-  {
-    // the walk order's groups, split into `shards` contiguous ranges
-    const long long gs = c->estimator == BH_EST_STOCHASTIC ? 32 : a.group;
-    const long long ng = (M + gs - 1) / gs;
-    a.g_begin = ng * c->shard / c->shards;
-    a.g_end = ng * (c->shard + 1) / c->shards;
-  }
+  const long long gs = walk_group_size(c, M);
+  const long long ng = (M + gs - 1) / gs;
+  // the walk order's groups, split into `shards` contiguous ranges
+  a.g_begin = ng * c->shard / c->shards;
+  a.g_end = ng * (c->shard + 1) / c->shards;
+  // whole calls of the deterministic walk record their groups' costs; the
+  // next call over the same groups takes them heaviest first
+  const bool record_costs = c->schedule && c->shards == 1 &&
+                            c->estimator != BH_EST_STOCHASTIC && ng <= c->cap_groups;
+  a.gcost = record_costs ? c->gcost : nullptr;
+  a.gorder = (record_costs && c->sched_now) ? c->gorder : nullptr;
+  if (e == cudaSuccess && a.gorder)
+    e = launch_group_order(c->gcost, ng, c->gorder, c->ctrl, c->num_sms, s);
   if (c->estimator == BH_EST_STOCHASTIC) {
     SbhArgs b;
     b.spm = c->spm;
@@ -366,6 +408,10 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
     if (e == cudaSuccess) e = launch_sbh(b, c->strata, c->strata_cap, c->ctrl, s);
   } else if (e == cudaSuccess) {
     e = launch_walk(a, c->ctrl, s);
+    if (a.gcost) {
+      c->sched_groups = ng;
+      c->sched_gs = (int)gs;
+    }
   }
   record(c, 8, s);
   *fb_out = fb;
@@ -426,6 +472,8 @@ int bh_destroy(bh_ctx *c) {
     free_dev(c->stage_in);
     free_dev(c->stage_tgt);
     free_dev(c->stage_out);
+    free_dev(c->gcost);
+    free_dev(c->gorder);
     for (int i = 0; i <= BH_NUM_STAGES; ++i)
       if (c->ev[i]) cudaEventDestroy(c->ev[i]);
     if (c->gexec) cudaGraphExecDestroy(c->gexec);
@@ -495,6 +543,10 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       if (v < 0 || v >= c->shards) return fail(c, BH_EINVAL, "shard must be in 0..shards-1");
       c->shard = (int)v;
       return BH_OK;
+    case BH_OPT_SCHEDULE:
+      if (v < 0 || v > 2) return fail(c, BH_EINVAL, "schedule must be 0, 1 or 2");
+      c->schedule = (int)v;
+      return BH_OK;
     case BH_OPT_ORDER:
       if (v != BH_ORDER_RADIX && v != BH_ORDER_TREE) return fail(c, BH_EINVAL, "unknown order");
       c->order = (int)v;
@@ -541,6 +593,14 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   if (c->order == BH_ORDER_TREE &&
       (rc = ensure_order(c, c->cap_n > c->cap_m ? c->cap_n : c->cap_m)) != BH_OK)
     return rc;
+  if ((rc = ensure_sched(c, M)) != BH_OK) return rc;
+  const long long walk_gs = walk_group_size(c, M);
+  const long long walk_ng = (M + walk_gs - 1) / walk_gs;
+  const bool costs = c->schedule && c->shards == 1 && c->estimator != BH_EST_STOCHASTIC;
+  // with no more groups than the walk has warps taking them (16 per SM) every
+  // group starts at once and the order cannot matter (unless forced)
+  c->sched_now = costs && c->sched_groups == walk_ng && c->sched_gs == walk_gs &&
+                 (c->schedule == 2 || walk_ng > 16LL * c->num_sms);
   if (c->estimator == BH_EST_STOCHASTIC && !c->strata) {
     // strata of level s <= 6 number at most 8^6
     if (!alloc_dev(c->strata, 1LL << 18)) return fail(c, BH_ENOMEM, "strata list");
@@ -571,6 +631,8 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.strata_level = c->strata_level; key.seed = c->seed; key.pipeline = c->pipeline;
   key.order = c->order;
   key.shards = c->shards; key.shard = c->shard;
+  key.cap_groups = c->cap_groups;
+  key.schedule = c->schedule; key.sched = c->sched_now ? 1 : 0;
   bool graph = c->use_graph && !c->timing && c->cap_stream;
   if (graph) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -618,6 +680,9 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   c->last_fb = fb;
   c->last_fbt = fbt;
   c->last_self = self;
+  c->last_groups = walk_ng;
+  c->last_costs = costs;
+  c->last_ordered = c->sched_now;
   c->last_valid = true;
   return BH_OK;
 }
@@ -860,6 +925,17 @@ int bh_debug_export(bh_ctx *c, int what, void *dst, size_t bytes) {
       if (!need(4 * (size_t)c->last_m)) return fail(c, BH_EINVAL, "buffer too small");
       e = cudaMemcpy(dst, c->sort_t.idx[c->last_fbt], 4 * (size_t)c->last_m, cudaMemcpyDeviceToHost);
       break;
+    case BH_EXPORT_GROUP_COST:
+    case BH_EXPORT_GROUP_ORDER: {
+      const bool cost = what == BH_EXPORT_GROUP_COST;
+      if (cost ? !c->last_costs : !c->last_ordered)
+        return fail(c, BH_EINVAL, cost ? "last call recorded no group costs"
+                                       : "last call walked its groups in Morton order");
+      if (!need(4 * (size_t)c->last_groups)) return fail(c, BH_EINVAL, "buffer too small");
+      e = cudaMemcpy(dst, cost ? c->gcost : c->gorder, 4 * (size_t)c->last_groups,
+                     cudaMemcpyDeviceToHost);
+      break;
+    }
     case BH_EXPORT_WALK_STATS:
       if (!need(32)) return fail(c, BH_EINVAL, "buffer too small");
       memcpy(dst, st.walk_stats, 32);

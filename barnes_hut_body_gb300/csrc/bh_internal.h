@@ -123,6 +123,8 @@ struct StepCtrl {
   unsigned int trie_nodes;                 // insertion tree: nodes allocated
   unsigned int order_fail;                 // insertion tree: a row left out
   int pad1;
+  unsigned int sched_cnt[33];              // group schedule: groups per cost class
+  unsigned int sched_fill[33];             //   and positions handed out per class
 };
 
 // Control block kept across calls.
@@ -232,8 +234,17 @@ struct WalkArgs {
   int num_sms;
   int pipelined;              // producer/consumer warps (groups of 64)
   long long g_begin, g_end;   // the groups this call walks (a shard of them)
+  unsigned int *gcost;        // if set: per group, the terms its walk evaluates
+  const unsigned int *gorder; // if set: ticket k walks group gorder[k] (a
+                              // permutation of [0, g_end); g_begin is 0)
 };
 cudaError_t launch_walk(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s);
+// Heaviest first: order[] = the groups [0, ngroups) by descending power-of-two
+// class of cost[] (the previous walk's terms per group).  Two grid passes
+// (class counts, then placement) on counters in ctrl->step.
+cudaError_t launch_group_order(const unsigned int *cost, long long ngroups,
+                               unsigned int *order, DevCtrl *ctrl, int num_sms,
+                               cudaStream_t s);
 
 // Stochastic Barnes-Hut walk (one warp per 32 Morton-ordered queries).
 struct SbhArgs {

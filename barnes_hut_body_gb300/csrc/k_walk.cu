@@ -199,6 +199,14 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
     if (lane == 0) g = atomicAdd(&ctrl->step.work_ctr, 1u);
     g = __shfl_sync(0xffffffffu, g, 0) + (unsigned long long)a.g_begin;
     if ((long long)g >= gend) break;
+    if (a.gorder) {
+      g = a.gorder[g];
+      if ((long long)g >= gend) {        // not a permutation: skip, flag
+        if (lane == 0) set_err(ctrl, kErrOverflow);
+        continue;
+      }
+    }
+    const unsigned long long exec0 = executed;
     const long long t0 = (long long)g * GS;
     const int nvalid = (int)((a.m - t0) < GS ? (a.m - t0) : GS);
 
@@ -478,6 +486,10 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
         a.out[ci] = make_float4(a.G * (x0 + x1), a.G * (y0 + y1), a.G * (z0 + z1),
                                 a.G * ph);
     }
+    if (a.gcost && lane == 0) {
+      const unsigned long long c = executed - exec0;
+      a.gcost[g] = c < 0xffffffffull ? (unsigned)c : 0xffffffffu;
+    }
     ++ngroup_done;
   }
   if (lane == 0) {
@@ -587,8 +599,15 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
   while (alive) {
     unsigned long long gg = 0;
     if (lane == 0) gg = atomicAdd(&ctrl->step.work_ctr, 1u);
-    const long long g = (long long)__shfl_sync(0xffffffffu, gg, 0) + a.g_begin;
+    long long g = (long long)__shfl_sync(0xffffffffu, gg, 0) + a.g_begin;
     if (g >= gend) break;
+    if (a.gorder) {
+      g = a.gorder[g];
+      if (g >= gend) {                    // not a permutation: skip, flag
+        if (lane == 0) set_err(ctrl, kErrOverflow);
+        continue;
+      }
+    }
     const long long t0 = g * GS;
 
     float px[T], py[T], pz[T];
@@ -815,7 +834,7 @@ template <int T, bool kEps0, bool kSelf>
 __device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, WsPairSmem &S) {
   const int lane = threadIdx.x & 31;
   constexpr int GS = 32 * T;
-  unsigned long long executed = 0;
+  unsigned long long executed = 0, exec0 = 0;
   // all buffers start empty
 #pragma unroll
   for (int k = 0; k < kWsBufs; ++k) mb_arrive(&S.empty[k]);
@@ -835,6 +854,7 @@ __device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, Ws
     if (h.group < 0) break;
     if (h.group != cur) {                 // first buffer of a new group
       cur = h.group;
+      exec0 = executed;
       const long long t0 = cur * GS;
       nvalid = (int)((a.m - t0) < GS ? (a.m - t0) : GS);
 #pragma unroll
@@ -854,6 +874,10 @@ __device__ __forceinline__ void ws_consumer(const WalkArgs &a, DevCtrl *ctrl, Ws
     }
     if (h.last) {
       const long long t0 = cur * GS;
+      if (a.gcost && lane == 0) {
+        const unsigned long long c = executed - exec0;
+        a.gcost[cur] = c < 0xffffffffull ? (unsigned)c : 0xffffffffu;
+      }
 #pragma unroll
       for (int k = 0; k < T; ++k) {
         const long long t = t0 + k * 32 + lane;
@@ -1024,6 +1048,85 @@ cudaError_t launch_count(const WalkArgs &a, unsigned int *counts, DevCtrl *ctrl,
   cudaMemsetAsync(&ctrl->step.useful, 0, sizeof(unsigned long long), s);
   count_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.rec, a.tpos, a.tperm, a.m, a.n,
                                                  a.self_mode, counts, ctrl);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Group schedule.  Groups differ in cost by an order of magnitude (a group of
+// Morton-consecutive targets that straddles a high-level cell boundary, or
+// sits next to a dense clump, opens far more of the tree), and tickets
+// handed out in Morton order leave the heaviest ones to start last: the walk
+// ends with a tail of a few long groups while most SMs idle.  Handing the
+// heaviest out first (largest-first list scheduling) shortens that tail; the
+// costs come from the previous call's walk over the same groups.  Only the
+// order in which groups are taken changes, so every result is unchanged.
+// ---------------------------------------------------------------------------
+constexpr int kOrderThreads = 256;
+constexpr int kCostClasses = 33;      // 0 and the 32 powers of two of a u32
+
+// class of a cost by its leading bit, heaviest first: [2^31, 2^32) -> 0,
+// [2^30, 2^31) -> 1, ..., 1 -> 31, 0 -> 32
+__device__ __forceinline__ int cost_class(unsigned c) { return __clz(c); }
+
+// Groups per class.  Lanes of one class (match.any) add with one atomic.
+__global__ void __launch_bounds__(kOrderThreads)
+group_class_count_kernel(const unsigned int *__restrict__ cost, long long ngroups,
+                         unsigned int *cnt) {
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * kOrderThreads;
+  for (long long base = (long long)blockIdx.x * kOrderThreads; base < ngroups; base += stride) {
+    const long long g = base + threadIdx.x;
+    const int cls = g < ngroups ? cost_class(cost[g]) : kCostClasses;
+    const unsigned peers = __match_any_sync(0xffffffffu, cls);
+    if (cls < kCostClasses && (peers & ((1u << lane) - 1u)) == 0u)
+      atomicAdd(&cnt[cls], (unsigned)__popc(peers));
+  }
+}
+
+// Placement: class k owns positions [start_k, start_k + cnt_k) with the
+// classes in order; each group takes the next free position of its class.
+// Every class hands out exactly cnt_k positions, so order[] is a
+// permutation of [0, ngroups) (the order within a class is arbitrary).
+__global__ void __launch_bounds__(kOrderThreads)
+group_place_kernel(const unsigned int *__restrict__ cost, long long ngroups,
+                   const unsigned int *__restrict__ cnt, unsigned int *fill,
+                   unsigned int *__restrict__ order) {
+  __shared__ unsigned int start[kCostClasses];
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  if (threadIdx.x == 0) {
+    unsigned run = 0;
+    for (int k = 0; k < kCostClasses; ++k) {
+      start[k] = run;
+      run += cnt[k];
+    }
+  }
+  __syncthreads();
+  const long long stride = (long long)gridDim.x * kOrderThreads;
+  for (long long base = (long long)blockIdx.x * kOrderThreads; base < ngroups; base += stride) {
+    const long long g = base + threadIdx.x;
+    const int cls = g < ngroups ? cost_class(cost[g]) : kCostClasses;
+    const unsigned peers = __match_any_sync(0xffffffffu, cls);
+    const int leader = __ffs(peers) - 1;
+    unsigned at = 0;
+    if (cls < kCostClasses && lane == leader) at = atomicAdd(&fill[cls], (unsigned)__popc(peers));
+    at = __shfl_sync(0xffffffffu, at, leader) + (unsigned)__popc(peers & lt);
+    if (cls < kCostClasses && at < cnt[cls]) order[start[cls] + at] = (unsigned)g;
+  }
+}
+
+cudaError_t launch_group_order(const unsigned int *cost, long long ngroups,
+                               unsigned int *order, DevCtrl *ctrl, int num_sms,
+                               cudaStream_t s) {
+  if (ngroups <= 0) return cudaSuccess;
+  long long blocks = (ngroups + kOrderThreads - 1) / kOrderThreads;
+  if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
+  group_class_count_kernel<<<(unsigned)blocks, kOrderThreads, 0, s>>>(cost, ngroups,
+                                                                        ctrl->step.sched_cnt);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  group_place_kernel<<<(unsigned)blocks, kOrderThreads, 0, s>>>(
+      cost, ngroups, ctrl->step.sched_cnt, ctrl->step.sched_fill, order);
   return cudaGetLastError();
 }
 

@@ -47,17 +47,22 @@ SM_MAX_MHZ = 2070.0
 ONE_BLOCK_SORT_MAX = 4096
 
 
-def kernels_per_step(order: str, n: int, m: int | None) -> int:
+def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152) -> int:
     """Our kernels per step with 63-bit keys: per particle set (n sources,
     and m separate targets unless m is None) bbox, keys and the order (8
     radix passes, or one kernel up to ONE_BLOCK_SORT_MAX keys, + gather; or
     the tree order's histogram, top levels, insert, node count, count and
-    place kernels); then build count/scan/write, centre of mass and walk."""
+    place kernels); then build count/scan/write, centre of mass, the group
+    schedule (on a repeated call with more walk groups than 16 per SM) and
+    walk."""
     def per_set(rows: int) -> int:
         if order != "radix":
             return 2 + 6
         return 2 + (1 if rows <= ONE_BLOCK_SORT_MAX else 8) + 1
-    return per_set(n) + (0 if m is None else per_set(m)) + 5
+    targets = n if m is None else m
+    groups = -(-targets // walk_group(targets))
+    scheduled = 2 if groups > 16 * sms else 0     # class counts, placement
+    return per_set(n) + (0 if m is None else per_set(m)) + 5 + scheduled
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 29.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
@@ -421,7 +426,8 @@ def run_ours(args, rank, local_rank, world):
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     achieved = exec_terms * FLOPS_PER_TERM / (walk_ms / 1e3) / 1e12
-    launches = kernels_per_step(args.order, src.shape[0], None if tgt is None else tgt.shape[0]) * args.steps
+    launches = kernels_per_step(args.order, src.shape[0], None if tgt is None else tgt.shape[0],
+                                props.multi_processor_count) * args.steps
 
     if rank == 0:
         cpu = None

@@ -85,6 +85,18 @@ typedef struct bh_ctx bh_ctx;
                                    1..2^20 (default 1), see below            */
 #define BH_OPT_SHARD        14  /* the shard the context's calls walk,
                                    0..shards-1 (default 0)                   */
+#define BH_OPT_SCHEDULE     15  /* 1 (default): a call over the same groups
+                                   as the previous call (same target count
+                                   and group size, one shard, Barnes-Hut
+                                   estimator) hands the groups to the walk
+                                   heaviest first, by the terms each group
+                                   evaluated in the previous call (two small
+                                   extra kernels), when there are more
+                                   groups than the walk takes at once (16 per
+                                   SM); 2: whenever it can, even then; 0:
+                                   Morton order.  The order changes no
+                                   result, only how the walk's tail of long
+                                   groups overlaps                           */
 #define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
                                    strata, 0..6 (default 2: up to 64 strata,
                                    the child count of the root of a tree with
@@ -188,6 +200,14 @@ typedef struct bh_ctx bh_ctx;
 #define BH_EXPORT_TARGET_PERM 7  /* uint32[m]: Morton order of the targets   */
 #define BH_EXPORT_WALK_STATS  8  /* uint64[4]: walk rounds, nodes tested,
                                     nodes decided by the vote, leaf chunks   */
+#define BH_EXPORT_GROUP_COST  9  /* uint32[groups]: terms each walk group
+                                    evaluated (targets x list entries), in
+                                    group (Morton) order; BH_EINVAL unless
+                                    the call recorded them (BH_OPT_SCHEDULE
+                                    1, one shard, Barnes-Hut estimator)     */
+#define BH_EXPORT_GROUP_ORDER 10 /* uint32[groups]: the order the call handed
+                                    its groups to the walk; BH_EINVAL if it
+                                    used Morton order                        */
 
 /* Stage indices for bh_get_stage_times. */
 #define BH_STAGE_BBOX      0
