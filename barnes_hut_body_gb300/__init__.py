@@ -42,7 +42,7 @@ EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
             "bh_set_debug", "bh_compute", "bh_compute_host", "bh_direct",
             "bh_sync_status", "bh_get_stage_times", "bh_get_counters",
             "bh_debug_export", "bh_count_interactions", "bh_direct_static",
-            "bh_leapfrog", "bh_neighbors", "bh_last_error")
+            "bh_leapfrog", "bh_neighbors", "bh_fp32_probe", "bh_last_error")
 
 _lib = None
 
@@ -78,6 +78,7 @@ def lib():
         L.bh_direct_static.argtypes = [vp, sz, vp, sz, f, f, vp, vp]
         L.bh_leapfrog.argtypes = [vp, vp, vp, sz, vp, f, i, i, vp]
         L.bh_neighbors.argtypes = [vp, vp, vp, sz, f, i, vp, vp, vp, sz, vp]
+        L.bh_fp32_probe.argtypes = [vp, i, i, C.POINTER(C.c_double), vp]
         L.bh_last_error.argtypes = [vp]
         L.bh_last_error.restype = C.c_char_p
         for name in EXPORTED:
@@ -184,6 +185,15 @@ def bh_direct_static(pos_mass, targets, acc_pot, G: float = 1.0, eps: float = 0.
     if rc != BH_OK:
         raise BHError(rc, "bh_direct_static failed (bad argument, more than "
                           "262144 targets, or a CUDA error)")
+
+
+def bh_fp32_probe(ctx, packed: bool, iters: int, stream) -> float:
+    """Enqueue one launch of the fp32 FMA-chain probe on `stream` (a
+    cudaStream_t as int); returns the fp32 flops that launch performs."""
+    fl = C.c_double(0.0)
+    _check(ctx, lib().bh_fp32_probe(ctx, 1 if packed else 0, int(iters), C.byref(fl),
+                                    C.c_void_p(stream)))
+    return fl.value
 
 
 def bh_leapfrog(ctx, pos_mass, vel, acc_pot, dt: float, nsteps: int,

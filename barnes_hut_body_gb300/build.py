@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbh.so")
 SOURCES = ["bh_api.cu", "k_keys_sort.cu", "k_build.cu", "k_walk.cu", "k_direct.cu",
-           "k_integrate.cu", "k_sbh.cu", "k_nbr.cu", "k_order.cu"]
+           "k_integrate.cu", "k_sbh.cu", "k_nbr.cu", "k_order.cu", "k_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -866,6 +866,21 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
   return BH_OK;
 }
 
+int bh_fp32_probe(bh_ctx *c, int packed, int iters, double *flops, void *stream) {
+  if (!c) return BH_EINVAL;
+  c->err.clear();
+  if ((packed != 0 && packed != 1) || iters < 1 || iters > (1 << 24))
+    return fail(c, BH_EINVAL, "fp32 probe: packed must be 0 or 1, iters in 1..2^24");
+  DeviceGuard g(c->device);
+  const int nsink = 4 * 2 * c->bbox_blocks;   // floats of c->partials, never written
+  cudaError_t e = launch_fma_probe(packed == 1, iters, c->num_sms,
+                                   reinterpret_cast<float *>(c->partials), nsink,
+                                   (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(c, e, "fp32 probe launch");
+  if (flops) *flops = (double)fma_probe_flops(packed == 1, iters, c->num_sms);
+  return BH_OK;
+}
+
 int bh_get_stage_times(bh_ctx *c, float *ms, int n) {
   if (!c || !ms || n < 0 || n > BH_NUM_STAGES) return BH_EINVAL;
   if (!c->timed) return fail(c, BH_EINVAL, "no timed call (set BH_OPT_TIMING)");

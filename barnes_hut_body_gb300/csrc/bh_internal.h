@@ -302,6 +302,12 @@ cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
                           double *partial, long long partial_cap, float4 *out,
                           int num_sms, cudaStream_t s);
 
+// fp32 throughput probe (k_peak.cu): flops one launch performs, and the
+// launch (8 blocks of 256 threads per SM; `sink` is never written).
+long long fma_probe_flops(bool packed, int iters, int num_sms);
+cudaError_t launch_fma_probe(bool packed, int iters, int num_sms, float *sink,
+                             int nsink, cudaStream_t s);
+
 cudaError_t launch_kick_drift(float4 *pm, float4 *vel, const float4 *acc,
                               long long n, float hk, float dt, int num_sms,
                               cudaStream_t s);

@@ -65,7 +65,7 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152) -> int:
     return per_set(n) + (0 if m is None else per_set(m)) + 5 + scheduled
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = 29.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
+WALK_TRAFFIC_BYTES = 29.91e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -224,6 +224,44 @@ def cpu_oracle_step(src, tgt, G, eps, theta, sample: int, leaf_cap: int = 16):
     return (t1 - t0) + (t2 - t1) * scale, float(terms.mean()) * m
 
 
+def cpu_oracle_stages(src, tgt, G, eps, theta, sample: int = 4096,
+                      direct_sample: int = 256, leaf_cap: int = 16) -> dict:
+    """The oracle's stages timed one by one (seconds for the whole problem):
+    bounding cube + Morton keys, stable sort + reorder, octree build, centre
+    of mass, the per-target walk of `sample` targets and the fp64 direct sum
+    of `direct_sample` targets, both scaled to all targets (the direct sum is
+    an extrapolation)."""
+    import numpy as np
+    import oracle as O
+    import workloads as W
+    t = [time.perf_counter()]
+    cube = O.bbox(src)
+    k = O.keys(src, cube, 21)
+    t.append(time.perf_counter())
+    perm = O.sort(k)
+    sk = k[perm]
+    spm = np.ascontiguousarray(src[perm])
+    t.append(time.perf_counter())
+    tree = O.build_tree(sk, 21, leaf_cap)
+    t.append(time.perf_counter())
+    O.com(spm, sk, tree, cube, 21)
+    t.append(time.perf_counter())
+    o = O.OracleBH(src, theta=theta, G=G, eps=eps, leaf_cap=leaf_cap)
+    m = src.shape[0] if tgt is None else tgt.shape[0]
+    idx = W.error_sample(m, sample, seed=5)
+    t.append(time.perf_counter())
+    o.bh(tgt, idx=idx)
+    t.append(time.perf_counter())
+    didx = idx[:min(direct_sample, idx.shape[0])]
+    o.direct(tgt, idx=didx)
+    t.append(time.perf_counter())
+    st = {"bbox_keys": t[1] - t[0], "sort_reorder": t[2] - t[1], "build": t[3] - t[2],
+          "com": t[4] - t[3], "walk": (t[6] - t[5]) * m / idx.shape[0],
+          "direct_extrapolated": (t[7] - t[6]) * m / didx.shape[0]}
+    st["step"] = st["bbox_keys"] + st["sort_reorder"] + st["build"] + st["com"] + st["walk"]
+    return {k: round(v, 4) for k, v in st.items()}
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle as it stands, on this workload."""
     if rank != 0:
@@ -257,6 +295,28 @@ def run_reference(args, rank, world):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def measured_fp32_tflops(ctx, stream, iters: int = 1 << 16, reps: int = 5) -> dict:
+    """Measured fp32 peak: the library's FMA-chain probe (bh_fp32_probe), in
+    scalar and packed (fma.rn.f32x2) form, 3 untimed launches then the best
+    of `reps`, each timed with CUDA events on the launching stream."""
+    import torch
+    import barnes_hut_body_gb300 as B
+    out = {}
+    for name, packed in (("scalar", False), ("packed", True)):
+        for _ in range(3):
+            flops = B.bh_fp32_probe(ctx, packed, iters, stream.cuda_stream)
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            B.bh_fp32_probe(ctx, packed, iters, stream.cuda_stream)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out[name] = flops / (best / 1e3) / 1e12
+    return out
 
 
 def measured_hbm_gbs() -> float:
@@ -426,6 +486,8 @@ def run_ours(args, rank, local_rank, world):
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     achieved = exec_terms * FLOPS_PER_TERM / (walk_ms / 1e3) / 1e12
+    probe = measured_fp32_tflops(bh.ctx, stream)
+    peak_meas = max(probe.values())
     launches = kernels_per_step(args.order, src.shape[0], None if tgt is None else tgt.shape[0],
                                 props.multi_processor_count) * args.steps
 
@@ -434,10 +496,21 @@ def run_ours(args, rank, local_rank, world):
         if not args.no_cpu_baseline and world == 1:
             import oracle as O
             s, u = cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
-            cpu = {"value": u / s, "unit": "interactions/s", "cores": O.num_threads(),
+            cores = O.num_threads()
+            stages = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
+            O.set_threads(1)
+            stages1 = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
+            O.set_threads(cores)
+            cpu = {"value": u / s, "unit": "interactions/s", "cores": cores,
                    "kind": "oracle",
                    "sample": f"build over all {src.shape[0]} sources + per-target walk of "
-                             f"{min(args.cpu_sample, m)} sampled targets, walk time scaled to {m}"}
+                             f"{min(args.cpu_sample, m)} sampled targets, walk time scaled to {m}",
+                   "stages_s": stages,
+                   "one_core": {"value": u / stages1["step"], "cores": 1, "stages_s": stages1},
+                   "stages_note": "each stage timed alone over the whole problem; walk of "
+                                  f"{min(args.cpu_sample, m)} and fp64 direct sum of "
+                                  f"{min(256, m)} sampled targets, scaled to {m} "
+                                  "(direct: extrapolated)"}
         line = {
             "metric": "useful_interactions_per_s", "value": value, "unit": "interactions/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -456,7 +529,9 @@ def run_ours(args, rank, local_rank, world):
                          "traffic": traffic,
                          "kernel": "walk_kernel<2,vote>" if args.fused_walk
                                    else "walk_ws_kernel<2,vote>",
-                         "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz"},
+                         "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz",
+                         "peak_measured": peak_meas, "frac_measured": achieved / peak_meas,
+                         "probe_tflops": probe},
             "e2e": {"value": total_useful / (e2e_ms / 1e3), "unit": "interactions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches,
@@ -507,6 +582,8 @@ def run_direct(args, rank, local_rank, world):
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     achieved = pairs * FLOPS_PER_TERM / (ms / 1e3) / 1e12
+    probe = measured_fp32_tflops(bh.ctx, stream)
+    peak_meas = max(probe.values())
     if rank == 0:
         print(json.dumps({
             "metric": "direct_pairs_per_s", "value": sum_over_ranks(pairs, world, device) / (ms / 1e3),
@@ -516,7 +593,10 @@ def run_direct(args, rank, local_rank, world):
             "config": {"workload": args.workload, "n_sources": n, "n_targets": m, "eps": eps,
                        "kernel": "direct (fp32 tiles, fp64 across tiles)"},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None},
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz",
+                         "peak_measured": peak_meas, "frac_measured": achieved / peak_meas,
+                         "probe_tflops": probe},
             "gpu_launches": 2 * args.steps}), flush=True)
     bh.close()
     return 0

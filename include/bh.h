@@ -377,6 +377,19 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
                  void *stream);
 
 /*
+ * fp32 throughput probe, for the roofline of the walk and direct-sum
+ * kernels (bound by fp32 arithmetic); a calibration aid with no counterpart
+ * in the pages.  Enqueues on `stream` one launch of a kernel whose threads
+ * (2048 per SM) run 8 independent fused multiply-add chains for `iters`
+ * steps, touching no memory: packed = 0 uses scalar fma.rn.f32, packed = 1
+ * the packed fma.rn.f32x2 (two lane-FMAs per instruction).  `flops` (host,
+ * or NULL) receives the fp32 flops of that launch, 2 per lane-FMA; time the
+ * launch with events on `stream` and divide.  iters in 1..2^24, else
+ * BH_EINVAL; BH_ECUDA if the launch fails.  Does not synchronise.
+ */
+int bh_fp32_probe(bh_ctx *c, int packed, int iters, double *flops, void *stream);
+
+/*
  * Per-stage milliseconds of the last bh_compute made with BH_OPT_TIMING on
  * (indices BH_STAGE_*; a stage that did not run reads 0).  Synchronises on
  * the last recorded event.  n = number of floats at ms (<= BH_NUM_STAGES).

@@ -67,6 +67,7 @@ def test_calls_without_a_device_fail_cleanly(bhmod):
     assert L.bh_neighbors(None, None, None, 0, 2.0, 1, None, None, None, 0, None) == bhmod.BH_EINVAL
     assert L.bh_leapfrog(None, None, None, 0, None, 1e-3, 1, 0, None) == bhmod.BH_EINVAL
     assert L.bh_set_option(None, bhmod.BH_OPT_ESTIMATOR, 1) == bhmod.BH_EINVAL
+    assert L.bh_fp32_probe(None, 0, 1, None, None) == bhmod.BH_EINVAL
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -123,6 +123,36 @@ def test_bad_arguments(B):
         bh.compute(base[1:].view(10, 4))
 
 
+def test_fp32_probe(B):
+    """The FMA-chain probe runs, counts its flops from the launch shape, and
+    its rate is physical: the scalar form at most the formula peak (SMs x
+    128 lanes x 2 flop x 2070 MHz), neither form implausibly slow."""
+    import torch
+    bh = B.BarnesHut()
+    stream = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    formula = sms * 128 * 2 * 2070e6
+    iters = 1 << 14
+    for packed in (False, True):
+        flops = B.bh_fp32_probe(bh.ctx, packed, iters, stream.cuda_stream)
+        assert flops == sms * 2048 * iters * 8 * (2 if packed else 1) * 2
+        best = float("inf")
+        for _ in range(4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            B.bh_fp32_probe(bh.ctx, packed, iters, stream.cuda_stream)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        rate = flops / best
+        assert 0.2 * formula < rate < (1.05 if not packed else 2.1) * formula, (packed, rate)
+    assert bh.status() == 0
+    with pytest.raises(B.BHError):
+        B.bh_fp32_probe(bh.ctx, False, 0, stream.cuda_stream)
+    with pytest.raises(B.BHError):
+        B.bh_fp32_probe(bh.ctx, False, (1 << 24) + 1, stream.cuda_stream)
+
+
 def test_host_buffers_match_device(B):
     import torch
     src = W.plummer(50000, seed=7)
