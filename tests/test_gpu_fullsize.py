@@ -3,6 +3,8 @@ bench.py times (theta 0.5, vote opening, groups of 64, leaf capacity 16,
 63-bit keys): keys, permutation and tree bit-exact against the oracle on the
 whole problem; forces on sampled targets (the oracle walks them one by one)
 and on sampled groups (the oracle's group walk with the same rule)."""
+import functools
+
 import numpy as np
 import pytest
 
@@ -27,9 +29,14 @@ def _check_full(name, src, tgt, G, eps, theta, sample, ngroups_sample=256):
     direct = o.direct(tgt, idx=idx)
     per_target, _ = o.bh(tgt, idx=idx)
     g, ostats = H.assert_error_no_worse(got[idx], per_target, direct, name)
-    ng = (m + 63) // 64
+    # the default group size: 64, or 32 when there are too few targets to
+    # fill the GPU with groups of 64 (read back from the number walked)
+    import barnes_hut_body_gb300 as B
+    _, walked = B.bh_get_counters(bh.ctx)
+    gs = 32 if walked == (m + 31) // 32 and m > 32 else 64
+    ng = (m + gs - 1) // gs
     gsel = np.sort(W.rng(13).choice(ng, size=min(ngroups_sample, ng), replace=False))
-    ref, rows, _, mag = o.bh_group(tgt, group=64, mode=0, groups=gsel, with_abs=True)
+    ref, rows, _, mag = o.bh_group(tgt, group=gs, mode=0, groups=gsel, with_abs=True)
     H.assert_walk_close(got[rows], ref, name, mag)
     return g, ostats
 
@@ -51,7 +58,34 @@ def test_surface_2e20_with_grid_targets():
     _check_full("surface2e20", src, tgt, 1.0, 1e-4, 0.5, 4096, 128)
 
 
-@pytest.mark.parametrize("theta", [0.3, 0.8])
+@functools.lru_cache(maxsize=2)
+def _plummer(log2n):
+    return W.plummer(1 << log2n, seed=4)
+
+
+@pytest.mark.parametrize("theta", [0.3, 0.5, 0.8])
 def test_plummer_2e22(theta):
-    src = W.plummer(1 << 22, seed=4)
+    src = _plummer(22)
     _check_full("plummer2e22", src, None, 1.0, 1e-3, theta, 2048, 64)
+
+
+@pytest.mark.parametrize("theta", [0.3, 0.5, 0.8])
+@pytest.mark.parametrize("log2n", [16, 18, 20])
+def test_plummer_sweep(log2n, theta):
+    """The Plummer scaling sweep's sizes below 2^22 at every theta."""
+    src = _plummer(log2n)
+    _check_full(f"plummer2e{log2n}", src, None, 1.0, 1e-3, theta, 2048, 64)
+
+
+def test_plummer_2e24():
+    """The sweep's largest size, 16,777,216 particles (theta 0.5)."""
+    src = W.plummer(1 << 24, seed=4)
+    _check_full("plummer2e24", src, None, 1.0, 1e-3, 0.5, 1024, 32)
+
+
+@pytest.mark.parametrize("log2m", [15, 17])
+def test_surface_with_grid_targets(log2m):
+    """The source/target workload's smaller source counts, 10^6 grid targets."""
+    src = W.ellipsoid_surfaces(1 << log2m, seed=2)
+    tgt = W.query_grid(src)
+    _check_full(f"surface2e{log2m}", src, tgt, 1.0, 1e-4, 0.5, 4096, 128)
