@@ -28,6 +28,7 @@ BH_OPT_PIPELINE = 11
 BH_OPT_ORDER = 12
 BH_OPT_SHARDS, BH_OPT_SHARD = 13, 14
 BH_OPT_SCHEDULE = 15
+BH_OPT_TARGET_KEY_BITS = 16
 BH_ORDER_RADIX, BH_ORDER_TREE = 0, 1
 BH_EST_BARNES_HUT, BH_EST_STOCHASTIC = 0, 1
 BH_OPEN_VOTE, BH_OPEN_BOX = 0, 1
@@ -339,7 +340,8 @@ _OPTION_KEYS = dict(key_bits=BH_OPT_KEY_BITS, leaf_cap=BH_OPT_LEAF_CAP,
                     graph=BH_OPT_GRAPH, estimator=BH_OPT_ESTIMATOR, seed=BH_OPT_SEED,
                     samples=BH_OPT_SAMPLES, strata_level=BH_OPT_STRATA_LEVEL,
                     pipeline=BH_OPT_PIPELINE, order=BH_OPT_ORDER, shards=BH_OPT_SHARDS,
-                    shard=BH_OPT_SHARD, schedule=BH_OPT_SCHEDULE)
+                    shard=BH_OPT_SHARD, schedule=BH_OPT_SCHEDULE,
+                    target_key_bits=BH_OPT_TARGET_KEY_BITS)
 
 
 class BarnesHut:

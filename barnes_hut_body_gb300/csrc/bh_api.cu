@@ -27,6 +27,7 @@ struct bh_ctx {
   int num_sms = 1;
   float theta = 0.5f, G = 1.f, eps = 0.f;
   int bits = 21, leaf_cap = 16, opening = BH_OPEN_VOTE, timing = 0, group = 0;
+  int tbits = 10;                   // BH_OPT_TARGET_KEY_BITS
   int estimator = BH_EST_BARNES_HUT, samples = 1, strata_level = 2;
   int pipeline = 1;
   int order = BH_ORDER_RADIX;
@@ -83,7 +84,7 @@ struct bh_ctx {
     void *out;
     long long n, m, cap_n, cap_m, cap_order, cap_groups;   // capacities: buffers reallocated
     float theta, G, eps;
-    int bits, leaf_cap, opening, group;
+    int bits, tbits, leaf_cap, opening, group;
     unsigned spin;
     int estimator, samples, strata_level, pipeline, order, shards, shard, schedule, sched;
     unsigned long long seed;
@@ -311,19 +312,19 @@ namespace {
 // key order in `sorted`.  Radix sort then gather, or (BH_ORDER_TREE) the
 // insertion tree's depth-first order, which writes the rows itself.  Event
 // `rec` (if >= 0) is recorded between ordering and placement.
-cudaError_t enqueue_order(bh_ctx *c, const float4 *pm, long long n, SortBufs &sb,
+cudaError_t enqueue_order(bh_ctx *c, const float4 *pm, long long n, int bits, SortBufs &sb,
                           float4 *sorted, int which, int rec, int *fb, cudaStream_t s) {
   cudaError_t e;
   if (c->order == BH_ORDER_TREE) {
     *fb = 1;
-    e = launch_order_tree(pm, sb.keys[0], n, c->bits, c->order_bufs, sb.keys[1], sb.idx[1],
+    e = launch_order_tree(pm, sb.keys[0], n, bits, c->order_bufs, sb.keys[1], sb.idx[1],
                           sorted, c->ctrl, c->num_sms, s);
     if (rec >= 0) record(c, rec, s);
     if (e == cudaSuccess)
-      e = launch_order_place(pm, sb.keys[0], n, c->bits, c->order_bufs, sb.keys[1],
+      e = launch_order_place(pm, sb.keys[0], n, bits, c->order_bufs, sb.keys[1],
                              sb.idx[1], sorted, c->ctrl, c->num_sms, s);
   } else {
-    e = launch_sort(sb, n, c->bits, c->ctrl, which, c->spin_limit, fb, s);
+    e = launch_sort(sb, n, bits, c->ctrl, which, c->spin_limit, fb, s);
     if (rec >= 0) record(c, rec, s);
     if (e == cudaSuccess) e = launch_gather(pm, sb.idx[*fb], n, sorted, s);
   }
@@ -343,7 +344,7 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   record(c, 1, s);
   if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
   record(c, 2, s);
-  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->sort, c->spm, 0, 3, &fb, s);
+  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->bits, c->sort, c->spm, 0, 3, &fb, s);
   else record(c, 3, s);
   record(c, 4, s);
   if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
@@ -351,9 +352,9 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   if (e == cudaSuccess) e = launch_com(c->spm, c->sort.keys[fb], N, c->bits, c->theta, c->build, c->ctrl, s);
   record(c, 6, s);
   if (!self) {
-    if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->bits, false, s);
-    if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->bits, s);
-    if (e == cudaSuccess) e = enqueue_order(c, tg, M, c->sort_t, c->stm, 1, -1, &fbt, s);
+    if (e == cudaSuccess) e = launch_bbox(tg, M, c->partials, c->bbox_blocks, c->ctrl, 1, c->tbits, false, s);
+    if (e == cudaSuccess) e = launch_keys(tg, M, c->sort_t.keys[0], c->ctrl, 1, c->tbits, s);
+    if (e == cudaSuccess) e = enqueue_order(c, tg, M, c->tbits, c->sort_t, c->stm, 1, -1, &fbt, s);
   }
   record(c, 7, s);
   WalkArgs a;
@@ -543,6 +544,10 @@ int bh_set_option(bh_ctx *c, int key, long long v) {
       if (v < 0 || v >= c->shards) return fail(c, BH_EINVAL, "shard must be in 0..shards-1");
       c->shard = (int)v;
       return BH_OK;
+    case BH_OPT_TARGET_KEY_BITS:
+      if (v != 21 && v != 10) return fail(c, BH_EINVAL, "target key bits must be 21 or 10");
+      c->tbits = (int)v;
+      return BH_OK;
     case BH_OPT_SCHEDULE:
       if (v < 0 || v > 2) return fail(c, BH_EINVAL, "schedule must be 0, 1 or 2");
       c->schedule = (int)v;
@@ -625,7 +630,8 @@ int bh_compute(bh_ctx *c, const float *pos_mass, size_t n, const float *targets,
   key.cap_n = c->cap_n; key.cap_m = c->cap_m;
   key.cap_order = c->order_bufs.cap_nodes;
   key.theta = c->theta; key.G = c->G; key.eps = c->eps;
-  key.bits = c->bits; key.leaf_cap = c->leaf_cap; key.opening = c->opening;
+  key.bits = c->bits; key.tbits = c->tbits; key.leaf_cap = c->leaf_cap;
+  key.opening = c->opening;
   key.group = c->group; key.spin = c->spin_limit;
   key.estimator = c->estimator; key.samples = c->samples;
   key.strata_level = c->strata_level; key.seed = c->seed; key.pipeline = c->pipeline;
@@ -843,7 +849,7 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
   cudaError_t e = cudaMemsetAsync(&c->ctrl->step, 0, sizeof(StepCtrl), s);
   if (e == cudaSuccess) e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
   if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
-  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->sort, c->spm, 0, -1, &fb, s);
+  if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->bits, c->sort, c->spm, 0, -1, &fb, s);
   if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
   NbArgs a;
   a.spm = c->spm;

@@ -372,6 +372,7 @@ def workload_config(name, src, tgt, theta, eps, order="radix", fused=False):
             "theta": theta, "eps": eps, "opening": f"warp vote, groups of {walk_group(m)}",
             "walk": "fused" if fused else "producer/consumer warp pairs",
             "leaf_cap": 16, "key_bits": 63, "order": order,
+            **({} if tgt is None else {"target_key_bits": 30}),
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
 
 

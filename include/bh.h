@@ -97,6 +97,15 @@ typedef struct bh_ctx bh_ctx;
                                    Morton order.  The order changes no
                                    result, only how the walk's tail of long
                                    groups overlaps                           */
+#define BH_OPT_TARGET_KEY_BITS 16 /* separate targets: bits per axis of the
+                                   Morton key that orders them, 10 (30-bit
+                                   keys, default: 4 radix passes) or 21.
+                                   The order only decides which targets
+                                   share a walk group; 2^10 cells per axis
+                                   already separate any group of 64 that is
+                                   spread over more than a 1/1024 of the
+                                   targets' cube, and targets in one cell
+                                   keep their input order               */
 #define BH_OPT_STRATA_LEVEL 10  /* stochastic estimator: octree level s of the
                                    strata, 0..6 (default 2: up to 64 strata,
                                    the child count of the root of a tree with

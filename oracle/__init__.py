@@ -202,8 +202,10 @@ class OracleBH:
     ``bh_group`` walks it per group of consecutive Morton-ordered targets.
     """
 
-    def __init__(self, src, theta=0.5, G=1.0, eps=1e-3, bits=21, leaf_cap=1):
+    def __init__(self, src, theta=0.5, G=1.0, eps=1e-3, bits=21, leaf_cap=1,
+                 target_bits=10):
         self.src = _rows(src)
+        self.target_bits = int(target_bits)
         self.n = self.src.shape[0]
         self.theta, self.G, self.eps = float(theta), float(G), float(eps)
         self.bits, self.leaf_cap = int(bits), int(leaf_cap)
@@ -251,11 +253,15 @@ class OracleBH:
         return out, terms
 
     def target_order(self, tgt=None):
-        """Morton order of the targets (the sources' own order in self mode)."""
+        """Morton order of the targets (the sources' own order in self mode).
+
+        Separate targets are ordered by Morton keys of ``target_bits`` bits
+        per axis on their own bounding cube (10 by default: the order only
+        decides which targets share a group walk), ties by index."""
         if tgt is None:
             return self.perm.astype(np.int64)
         t = _rows(tgt)
-        return sort(keys(t, bbox(t), self.bits)).astype(np.int64)
+        return sort(keys(t, bbox(t), self.target_bits)).astype(np.int64)
 
     def bh_group(self, tgt=None, group=32, mode=0, groups=None, theta=None,
                  with_abs=False):

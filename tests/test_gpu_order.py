@@ -65,7 +65,7 @@ def test_tree_order_of_separate_targets(B, name):
     bh_t, b, rc_t = H.gpu_bh(src, tgt, order=B.BH_ORDER_TREE, graph=0)
     assert rc_r == 0 and rc_t == 0
     m = tgt.shape[0]
-    ref = O.sort(O.keys(tgt, O.bbox(tgt), 21))
+    ref = O.sort(O.keys(tgt, O.bbox(tgt), 10))     # targets: 30-bit keys by default
     np.testing.assert_array_equal(B.bh_debug_export(bh_t.ctx, B.BH_EXPORT_TARGET_PERM, m), ref)
     np.testing.assert_array_equal(a, b)
     bh_r.close()

@@ -69,14 +69,15 @@ def test_permutation_bit_exact_around_the_one_block_sort(n, bits):
     bh.close()
 
 
+@pytest.mark.parametrize("tbits", [10, 21])
 @pytest.mark.parametrize("m", [7, 4096, 4097])
-def test_target_permutation_around_the_one_block_sort(m):
+def test_target_permutation_around_the_one_block_sort(m, tbits):
     import barnes_hut_body_gb300 as B
     src = SETS["uniform4096"]
     tgt = _dup_points(m, seed=m + 1)
-    bh, _, rc = H.gpu_bh(src, tgt)
+    bh, _, rc = H.gpu_bh(src, tgt, target_key_bits=tbits)
     assert rc == 0
-    ref = O.sort(O.keys(tgt, O.bbox(tgt), 21))
+    ref = O.sort(O.keys(tgt, O.bbox(tgt), tbits))
     np.testing.assert_array_equal(B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, m), ref)
     bh.close()
 
@@ -194,15 +195,18 @@ def test_theta_zero_is_the_direct_sum():
     H.assert_direct_close(got[idx], O.direct(src, None, 1.0, 1e-3, idx=idx))
 
 
-@pytest.mark.parametrize("opening", [0, 1])
-def test_source_target_walk(opening):
+@pytest.mark.parametrize("opening,tbits", [(0, 10), (1, 10), (0, 21)])
+def test_source_target_walk(opening, tbits):
     src = W.ellipsoid_surfaces(1 << 15, seed=2)
     tgt = W.query_grid(src, side=30)
-    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, G=1.0, eps=1e-4, opening=opening, group=64)
+    # a shuffled grid: the target order then comes from the keys alone
+    tgt = np.ascontiguousarray(tgt[np.random.default_rng(9).permutation(tgt.shape[0])])
+    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, G=1.0, eps=1e-4, opening=opening, group=64,
+                           target_key_bits=tbits)
     assert rc == 0
     import barnes_hut_body_gb300 as B
     tperm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, tgt.shape[0])
-    o = O.OracleBH(src, theta=0.5, G=1.0, eps=1e-4, leaf_cap=16)
+    o = O.OracleBH(src, theta=0.5, G=1.0, eps=1e-4, leaf_cap=16, target_bits=tbits)
     np.testing.assert_array_equal(tperm, o.target_order(tgt))
     ref, rows, _, mag = o.bh_group(tgt, group=64, mode=opening, with_abs=True)
     H.assert_walk_close(got[rows], ref, "surface", mag)
