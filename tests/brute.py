@@ -51,17 +51,51 @@ def cell_com(spm, first, count):
     return (p[:, :3] * p[:, 3:4]).sum(axis=0) / m, m
 
 
+def box_distance2(c, lo, hi, rule="box"):
+    """Squared distance from point c to the axis-aligned box [lo, hi].
+
+    rule "box" is the definition: the distance to the nearest point of the
+    box, which is c itself clipped into the box axis by axis (0 on an axis
+    where c lies between lo and hi).  The other rules are plausible mistakes,
+    kept only so the tests can show that their inputs tell them apart:
+    "far_corner" (distance to the farthest corner), "centre" (distance to the
+    box centre) and "swapped" (the clip written with lo and hi exchanged).
+    """
+    c = np.asarray(c, np.float64)
+    lo = np.asarray(lo, np.float64)
+    hi = np.asarray(hi, np.float64)
+    if rule == "box":
+        d = c - np.clip(c, lo, hi)
+    elif rule == "far_corner":
+        d = c - np.where(np.abs(c - lo) > np.abs(c - hi), lo, hi)
+    elif rule == "centre":
+        d = c - 0.5 * (lo + hi)
+    elif rule == "swapped":
+        d = np.array([hi[a] - c[a] if c[a] < hi[a] else (c[a] - lo[a] if c[a] > lo[a] else 0.0)
+                      for a in range(3)])
+    else:
+        raise ValueError(rule)
+    return float(d @ d)
+
+
 def recursive_bh(spm, skeys, bits, leaf_cap, L, theta, G, eps, x, self_j=-1,
-                 group_x=None):
+                 group_x=None, group_rule="vote", log=None):
     """Barnes-Hut by recursion over brute_cells.
 
-    group_x: optional (k,3) array; a cell is then accepted only if the test
-    holds for every row (the warp-vote form); the returned value is for x.
+    group_x: optional (k,3) array.  With group_rule "vote" a cell is then
+    accepted only if the test holds for every row (the warp-vote form); with
+    a box rule ("box", or one of the planted mistakes of box_distance2) only
+    if it holds at the distance from the centre of mass to the bounding box
+    of the rows.  The returned value is for x.  log: optional list that
+    receives (level, com, accepted) for every cell the walk decides.
     """
     cells = brute_cells(skeys, bits, leaf_cap)
     xs = np.asarray(x, np.float64)
     acc = np.zeros(4)
     terms = [0]
+    if group_x is not None:
+        gx = np.asarray(group_x, np.float64).reshape(-1, 3)
+        glo, ghi = gx.min(axis=0), gx.max(axis=0)
 
     def term(src_pos, m):
         d = np.asarray(src_pos, np.float64) - xs
@@ -78,9 +112,14 @@ def recursive_bh(spm, skeys, bits, leaf_cap, L, theta, G, eps, x, self_j=-1,
         f, c = cells[key]
         com, m = cell_com(spm, f, c)
         w = L / (2.0 ** lvl)
-        pts = [xs] if group_x is None else list(np.asarray(group_x, np.float64))
         ropen2 = (w * w) / (theta * theta) if theta > 0 else math.inf
-        ok = all(ropen2 < float((com - q) @ (com - q)) for q in pts)
+        if group_x is not None and group_rule != "vote":
+            ok = ropen2 < box_distance2(com, glo, ghi, group_rule)
+        else:
+            pts = [xs] if group_x is None else list(gx)
+            ok = all(ropen2 < float((com - q) @ (com - q)) for q in pts)
+        if log is not None:
+            log.append((lvl, com, ok))
         if ok:
             term(com, m)
         elif not is_internal(cells, key, bits, leaf_cap):

@@ -288,6 +288,68 @@ def test_group_walk_equals_recursive_vote(orc):
             np.testing.assert_allclose(out[r], ref, rtol=1e-12, atol=1e-14)
 
 
+def _box_group_case(orc, n, group, theta, seed):
+    p = W.uniform_cube(n, seed=seed)
+    o = orc.OracleBH(p, theta=theta, eps=1e-2, leaf_cap=2)
+    out, rows, _ = o.bh_group(group=group, mode=1)
+    return p, o, out, rows, o.target_order()
+
+
+def _box_group_brute(o, members, i, theta, rule, log=None):
+    ref, _ = brute.recursive_bh(o.spm, o.skeys, 21, 2, float(o.cube[3]), theta, 1.0, 1e-2,
+                                o.src[i, :3], self_j=int(o.rank[i]),
+                                group_x=o.src[members, :3], group_rule=rule, log=log)
+    return ref
+
+
+@pytest.mark.parametrize("n,group,theta,seed", [(64, 8, 0.6, 78), (128, 64, 0.5, 79)])
+def test_group_box_rule_equals_recursive_box(orc, n, group, theta, seed):
+    """The box opening rule with groups larger than one (so the box is a
+    real box, not a point): accept a cell iff w^2/theta^2 < d^2, d the
+    distance from its centre of mass to the nearest point of the group's
+    bounding box.  Every row equals the recursive restatement with that
+    rule; the same inputs under a plausible wrong distance (farthest corner,
+    box centre, the clip with lo and hi exchanged) give other results, and
+    the walks decide cells whose centre of mass lies inside the box on one
+    or two axes and outside on the others, where those rules part."""
+    p, o, out, rows, order = _box_group_case(orc, n, group, theta, seed)
+    wrong = {"far_corner": 0, "centre": 0, "swapped": 0}
+    partial = 0
+    for g0 in range(0, n, group):
+        members = order[g0:g0 + group]
+        lo = o.src[members, :3].astype(np.float64).min(axis=0)
+        hi = o.src[members, :3].astype(np.float64).max(axis=0)
+        for i in members:
+            log = []
+            ref = _box_group_brute(o, members, i, theta, "box", log)
+            r = int(np.nonzero(rows == i)[0][0])
+            np.testing.assert_allclose(out[r], ref, rtol=1e-12, atol=1e-14)
+            for lvl, com, ok in log:
+                inside = int(((com >= lo) & (com <= hi)).sum())
+                if inside in (1, 2):
+                    far = (float(o.cube[3]) / 2 ** lvl) ** 2 / theta ** 2 < \
+                        brute.box_distance2(com, lo, hi, "far_corner")
+                    partial += int(far != ok)
+            for rule in wrong:
+                bad = _box_group_brute(o, members, i, theta, rule)
+                wrong[rule] += int(not np.allclose(out[r], bad, rtol=1e-9, atol=1e-12))
+    assert partial > 0
+    for rule, nbad in wrong.items():
+        assert nbad > 0, rule
+
+
+def test_box_distance_definition():
+    """Hand cases of the distance to a box: inside (0), beside a face, off an
+    edge, off a corner, and inside on one axis only."""
+    lo, hi = np.array([0.0, 0.0, 0.0]), np.array([1.0, 2.0, 3.0])
+    assert brute.box_distance2([0.5, 1.0, 1.5], lo, hi) == 0.0
+    assert brute.box_distance2([1.5, 1.0, 1.5], lo, hi) == 0.25
+    assert brute.box_distance2([-1.0, 3.0, 1.5], lo, hi) == 2.0
+    assert brute.box_distance2([2.0, -2.0, 5.0], lo, hi) == 1.0 + 4.0 + 4.0
+    assert brute.box_distance2([0.5, 4.0, -1.0], lo, hi) == 4.0 + 1.0
+    assert brute.box_distance2([0.5, 4.0, -1.0], lo, hi, "far_corner") == 0.25 + 16.0 + 16.0
+
+
 def test_group_of_one_is_per_target(orc):
     p = W.uniform_cube(2000, seed=8)
     o = orc.OracleBH(p, theta=0.5, eps=1e-3, leaf_cap=4)
