@@ -177,12 +177,19 @@ def bh_direct_static(pos_mass, targets, acc_pot, G: float = 1.0, eps: float = 0.
     overlap on the GPU race.  The first call on a device should come before
     any stream capture.
     """
+    import torch
     p, n = _rows_ptr(pos_mass, "pos_mass")
     t, m = _rows_ptr(targets, "targets")
     o, k = _rows_ptr(acc_pot, "acc_pot")
     if k != (n if targets is None else m):
         raise ValueError("acc_pot has the wrong number of rows")
-    rc = lib().bh_direct_static(p, n, t, m, float(G), float(eps), o, _stream(pos_mass, stream))
+    dev = pos_mass.device
+    if acc_pot.device != dev or (targets is not None and targets.device != dev):
+        raise ValueError("pos_mass, targets and acc_pot must be on one device")
+    # the library finds its scratch array on the current device
+    with torch.cuda.device(dev):
+        rc = lib().bh_direct_static(p, n, t, m, float(G), float(eps), o,
+                                    _stream(pos_mass, stream))
     if rc != BH_OK:
         raise BHError(rc, "bh_direct_static failed (bad argument, more than "
                           "262144 targets, or a CUDA error)")

@@ -15,11 +15,18 @@
 // When there are too few targets to fill the GPU the sources are split over
 // blockIdx.y; every split writes its fp64 partial sums and a second kernel
 // adds the splits in a fixed order (deterministic).
+// Self mode: a block's 512 targets lie inside one 1024-row source tile; for
+// that tile alone the loop compares source and target indices and gives the
+// own pair no term at all (its reciprocal distance set to zero), so the
+// large m/eps of a small softening never enters a sum that must later
+// cancel it.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include <mutex>
+#include <tuple>
+#include <utility>
 
 #include "bh_internal.h"
 
@@ -30,6 +37,43 @@ namespace {
 constexpr int kDirThreads = 256;
 constexpr int kDirT = 2;
 constexpr int kDirTile = 1024;
+
+// One tile's sums for this thread's targets.  kMask: a source row equal to
+// a target's own row gets a zero reciprocal distance (no term).
+template <bool kMask, bool kEps0>
+__device__ __forceinline__ void tile_sum(const ulonglong2 (*tile)[2], int npairs,
+                                         const f2 *px, const f2 *py, const f2 *pz,
+                                         f2 e2, const long long *ti, long long b,
+                                         f2 *fx, f2 *fy, f2 *fz, f2 *fp) {
+#pragma unroll 4
+  for (int q = 0; q < npairs; ++q) {
+    const ulonglong2 a = tile[q][0], c = tile[q][1];    // (xx, yy), (zz, mm)
+#pragma unroll
+    for (int k = 0; k < kDirT; ++k) {
+      const f2 dx = sub2(a.x, px[k]), dy = sub2(a.y, py[k]), dz = sub2(c.x, pz[k]);
+      const f2 r2 = fma2(dx, dx, fma2(dy, dy, fma2(dz, dz, e2)));
+      float r0, r1;
+      upk(r2, r0, r1);
+      float i0 = rsqrt_ftz(r0), i1 = rsqrt_ftz(r1);
+      if (kEps0) {
+        i0 = (r0 > 0.f) ? i0 : 0.f;
+        i1 = (r1 > 0.f) ? i1 : 0.f;
+      }
+      if (kMask) {
+        const long long j = b + 2 * q;
+        i0 = (ti[k] == j) ? 0.f : i0;
+        i1 = (ti[k] == j + 1) ? 0.f : i1;
+      }
+      const f2 inv = pk(i0, i1);
+      const f2 minv = mul2(c.y, inv);
+      const f2 minv3 = mul2(minv, mul2(inv, inv));
+      fx[k] = fma2(dx, minv3, fx[k]);
+      fy[k] = fma2(dy, minv3, fy[k]);
+      fz[k] = fma2(dz, minv3, fz[k]);
+      fp[k] = sub2(fp[k], minv);
+    }
+  }
+}
 
 template <bool kSelf, bool kEps0>
 __global__ void __launch_bounds__(kDirThreads)
@@ -42,7 +86,6 @@ direct_kernel(const float4 *__restrict__ src, long long n,
   long long s1 = s0 + chunk;
   if (s1 > n) s1 = n;
   f2 px[kDirT], py[kDirT], pz[kDirT];   // targets, duplicated in both halves
-  float pm[kDirT];
   long long ti[kDirT];
   double acc[kDirT][4];
   const f2 e2 = pk(eps2, eps2);
@@ -51,7 +94,6 @@ direct_kernel(const float4 *__restrict__ src, long long n,
     ti[k] = tbase + k * kDirThreads + threadIdx.x;
     float4 p = __ldg(tgt + (ti[k] < m ? ti[k] : 0));
     px[k] = pk(p.x, p.x); py[k] = pk(p.y, p.y); pz[k] = pk(p.z, p.z);
-    pm[k] = p.w;
     acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.0;
   }
   for (long long b = s0; b < s1; b += kDirTile) {
@@ -70,29 +112,13 @@ direct_kernel(const float4 *__restrict__ src, long long n,
     f2 fx[kDirT], fy[kDirT], fz[kDirT], fp[kDirT];
 #pragma unroll
     for (int k = 0; k < kDirT; ++k) fx[k] = fy[k] = fz[k] = fp[k] = 0ull;
-#pragma unroll 4
-    for (int q = 0; q < npairs; ++q) {
-      const ulonglong2 a = tile[q][0], c = tile[q][1];    // (xx, yy), (zz, mm)
-#pragma unroll
-      for (int k = 0; k < kDirT; ++k) {
-        const f2 dx = sub2(a.x, px[k]), dy = sub2(a.y, py[k]), dz = sub2(c.x, pz[k]);
-        const f2 r2 = fma2(dx, dx, fma2(dy, dy, fma2(dz, dz, e2)));
-        float r0, r1;
-        upk(r2, r0, r1);
-        float i0 = rsqrt_ftz(r0), i1 = rsqrt_ftz(r1);
-        if (kEps0) {
-          i0 = (r0 > 0.f) ? i0 : 0.f;
-          i1 = (r1 > 0.f) ? i1 : 0.f;
-        }
-        const f2 inv = pk(i0, i1);
-        const f2 minv = mul2(c.y, inv);
-        const f2 minv3 = mul2(minv, mul2(inv, inv));
-        fx[k] = fma2(dx, minv3, fx[k]);
-        fy[k] = fma2(dy, minv3, fy[k]);
-        fz[k] = fma2(dz, minv3, fz[k]);
-        fp[k] = sub2(fp[k], minv);
-      }
-    }
+    // the tile holding this block's own rows (self mode, eps > 0)
+    const bool own = kSelf && !kEps0 && tbase < b + cnt &&
+                     b < tbase + kDirThreads * kDirT;
+    if (own)
+      tile_sum<true, kEps0>(tile, npairs, px, py, pz, e2, ti, b, fx, fy, fz, fp);
+    else
+      tile_sum<false, kEps0>(tile, npairs, px, py, pz, e2, ti, b, fx, fy, fz, fp);
 #pragma unroll
     for (int k = 0; k < kDirT; ++k) {
       float x0, x1, y0, y1, z0, z1, p0, p1;
@@ -100,13 +126,8 @@ direct_kernel(const float4 *__restrict__ src, long long n,
       upk(fy[k], y0, y1);
       upk(fz[k], z0, z1);
       upk(fp[k], p0, p1);
-      float ph = p0 + p1;
-      // self mode: the target's own row was in this tile and added
-      // m*rsqrt(eps^2) to -phi (and nothing to a); take it back out
-      if (kSelf && !kEps0 && ti[k] >= b && ti[k] < b + cnt)
-        ph += pm[k] * rsqrt_ftz(eps2);
       acc[k][0] += x0 + x1; acc[k][1] += y0 + y1;
-      acc[k][2] += z0 + z1; acc[k][3] += ph;
+      acc[k][2] += z0 + z1; acc[k][3] += p0 + p1;
     }
   }
 #pragma unroll
@@ -133,6 +154,22 @@ __global__ void direct_finish_kernel(const double *__restrict__ partial,
   }
 }
 
+// Launch with the status of this launch alone (cudaLaunchKernel returns it),
+// instead of reading the thread's last error, which may belong to an
+// earlier, unrelated call.
+template <typename... KArgs, size_t... I>
+cudaError_t launch_tuple(void (*k)(KArgs...), dim3 g, dim3 b, cudaStream_t s,
+                         std::tuple<KArgs...> &t, std::index_sequence<I...>) {
+  void *p[] = {(void *)&std::get<I>(t)...};
+  return cudaLaunchKernel((const void *)k, g, b, p, 0, s);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_checked(void (*k)(KArgs...), dim3 g, dim3 b, cudaStream_t s,
+                           Args... args) {
+  std::tuple<KArgs...> t(args...);
+  return launch_tuple(k, g, b, s, t, std::index_sequence_for<KArgs...>{});
+}
+
 }  // namespace
 
 cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
@@ -155,17 +192,15 @@ cudaError_t launch_direct(const float4 *src, long long n, const float4 *tgt,
   const float eps2 = eps * eps;
   dim3 grid((unsigned)bx, (unsigned)splits);
   const bool eps0 = eps2 == 0.f;
-  if (self_mode) {
-    if (eps0) direct_kernel<true, true><<<grid, kDirThreads, 0, s>>>(src, n, tgt, m, eps2, chunk, partial);
-    else direct_kernel<true, false><<<grid, kDirThreads, 0, s>>>(src, n, tgt, m, eps2, chunk, partial);
-  } else {
-    if (eps0) direct_kernel<false, true><<<grid, kDirThreads, 0, s>>>(src, n, tgt, m, eps2, chunk, partial);
-    else direct_kernel<false, false><<<grid, kDirThreads, 0, s>>>(src, n, tgt, m, eps2, chunk, partial);
-  }
+  auto k = self_mode ? (eps0 ? direct_kernel<true, true> : direct_kernel<true, false>)
+                     : (eps0 ? direct_kernel<false, true> : direct_kernel<false, false>);
+  cudaError_t e = launch_checked(k, grid, dim3(kDirThreads), s, src, n, tgt, m, eps2,
+                                 chunk, partial);
+  if (e != cudaSuccess) return e;
   long long fb = (m + 255) / 256;
   if (fb > (long long)num_sms * 16) fb = (long long)num_sms * 16;
-  direct_finish_kernel<<<(unsigned)fb, 256, 0, s>>>(partial, (int)splits, m, G, out);
-  return cudaGetLastError();
+  return launch_checked(direct_finish_kernel, dim3((unsigned)fb), dim3(256), s,
+                        (const double *)partial, (int)splits, m, G, out);
 }
 
 // ---------------------------------------------------------------------------

@@ -311,12 +311,17 @@ int bh_direct(bh_ctx *c, const float *pos_mass, size_t n,
  * It calls no cudaMalloc, cudaFree or other allocating routine.  Its only
  * scratch is a file-scope device array of 8 MiB (fp64 partial sums), held
  * by every GPU that loads the library until the process exits; at most
- * 262,144 targets per call (more returns BH_EINVAL).  The first call on a
- * device looks up the array's device address (make it before any stream
- * capture).  Every call shares the one array, so calls that overlap on the
- * GPU (other streams, other host threads) race and give wrong results;
- * serialise them.  Returns BH_OK, BH_EINVAL (bad pointer, alignment,
- * parameter or size) or BH_ECUDA.
+ * 262,144 targets per call (more returns BH_EINVAL).  It runs on the
+ * current CUDA device, which must be the device of every pointer.  The
+ * first call on a device looks up the array's device address (make it
+ * before any stream capture) and keeps it for the life of the process; a
+ * cudaDeviceReset of that device discards the array with the context, so
+ * the kept address is then stale: do not call this entry point on a device
+ * after the process has reset it.  Every call shares the one array, so
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * give wrong results; serialise them.  Returns BH_OK, BH_EINVAL (bad
+ * pointer, alignment, parameter or size) or BH_ECUDA (a failed look-up or
+ * launch of this call).
  */
 int bh_direct_static(const float *pos_mass, size_t n, const float *targets,
                      size_t m, float G, float eps, float *acc_pot,
