@@ -19,9 +19,16 @@ object reports the executed terms as fp32 FLOP/s (20 flops per term).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
 
-With N > 1 (launched by torch.distributed.run) every rank runs its own
-replica of the workload (the path has no exchange step); value is the sum of
-useful interactions over ranks divided by the slowest rank's time.
+With N > 1 (launched by torch.distributed.run) the ranks split one problem
+(--split targets, the default): every rank builds the whole tree from the
+replicated sources, walks its contiguous share of the Morton-ordered target
+groups, and an all-reduce of zero-filled result buffers gives every rank all
+rows in caller order, inside each timed step; value is the problem's useful
+interactions divided by the slowest rank's time ("scaling": "strong").
+--split replicas runs a whole replica per rank instead ("weak").
+
+The default run also times the 5,000,000-particle galaxy pair (reported
+under "also"); --also names other workloads, or none.
 """
 from __future__ import annotations
 
@@ -47,7 +54,8 @@ SM_MAX_MHZ = 2070.0
 ONE_BLOCK_SORT_MAX = 4096
 
 
-def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152) -> int:
+def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
+                     scheduled: bool = True) -> int:
     """Our kernels per step with 63-bit keys: per particle set (n sources,
     and m separate targets unless m is None) bbox, keys and the order (8
     radix passes, or one kernel up to ONE_BLOCK_SORT_MAX keys, + gather; or
@@ -61,8 +69,8 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152) -> int:
         return 2 + (1 if rows <= ONE_BLOCK_SORT_MAX else 8) + 1
     targets = n if m is None else m
     groups = -(-targets // walk_group(targets))
-    scheduled = 2 if groups > 16 * sms else 0     # class counts, placement
-    return per_set(n) + (0 if m is None else per_set(m)) + 5 + scheduled
+    sched = 2 if scheduled and groups > 16 * sms else 0     # class counts, placement
+    return per_set(n) + (0 if m is None else per_set(m)) + 5 + sched
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 29.91e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
@@ -80,6 +88,13 @@ def parse():
     ap.add_argument("--theta", type=float, default=None,
                     help="override the workload's opening angle")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workloads timed after the headline one and "
+                         "reported under 'also' (default galaxy5m with the default "
+                         "workload, else none)")
+    ap.add_argument("--split", choices=["targets", "replicas"], default="targets",
+                    help="N > 1: split one problem's target groups over the ranks "
+                         "(default), or run a whole replica per rank")
     ap.add_argument("--cpu-sample", type=int, default=4096,
                     help="targets the CPU oracle walks per baseline step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -331,25 +346,36 @@ def measured_hbm_gbs() -> float:
 
 def stage_bytes(n: int, m: int, nodes: int, self_mode: bool, order: str = "radix") -> dict:
     """Algorithmic DRAM bytes of each build-side stage for one step (63-bit
-    keys, 8 radix passes): what the stage must read and write at least.
-    The tree order's "sort" is the insertion tree: keys read, and per row at
-    least one 4-byte child slot written and its count and offset settled
-    (12 bytes); its "reorder" reads keys and rows and writes the sorted key,
-    index and row (8 + 16 in, 8 + 4 + 16 out)."""
+    keys, 8 radix passes): what the stage must read and write at least --
+    bbox 16 B per particle; keys 16 in + 8 out; a radix pass 24 B per
+    element; reorder 36; build 8 B per key + 32 B per node; centre of mass
+    16 B per particle + 32 B per node.  The tree order's "sort" is the
+    insertion tree: keys read, and per row at least one 4-byte child slot
+    written and its count and offset settled (12 bytes); its "reorder" reads
+    keys and rows and writes the sorted key, index and row (8 + 16 in,
+    8 + 4 + 16 out)."""
     sort = 8 * 24 * n if order == "radix" else 8 * n + 12 * n
     reorder = 4 * n + 16 * n + 16 * n if order == "radix" else 24 * n + 28 * n
     b = {
-        "bbox": 16 * n,                          # read particles
-        "keys": 16 * n + 8 * n,                  # read particles, write keys
-        "sort": sort,                            # radix: per pass key+index in and out
-        "reorder": reorder,                      # radix: perm, gather, write
-        "build": 2 * 8 * n + 25 * nodes,         # keys twice; topology written
-        "com": 16 * n + 69 * nodes,              # particles; topology in, records out
+        "bbox": 16 * n,
+        "keys": 16 * n + 8 * n,
+        "sort": sort,
+        "reorder": reorder,
+        "build": 8 * n + 32 * nodes,
+        "com": 16 * n + 32 * nodes,
     }
     if not self_mode:
         tsort = 8 * 24 * m + 36 * m if order == "radix" else 20 * m + 52 * m
         b["targets"] = 16 * m + 24 * m + tsort
     return b
+
+
+def kernel_bytes(n: int, m: int, nodes: int) -> dict:
+    """Bytes the build and centre-of-mass kernels move by their design: the
+    build reads the keys in its count and write passes and writes 25 B of
+    topology per node; the centre of mass reads the particles, 33 B of
+    topology per node and writes a 32-byte record and 4 more per node."""
+    return {"build": 2 * 8 * n + 25 * nodes, "com": 16 * n + 69 * nodes}
 
 
 def walk_group(m: int) -> int:
@@ -365,9 +391,13 @@ def walk_group(m: int) -> int:
     return 32 if (m + 63) // 64 < 16 * sms else 64
 
 
-def workload_config(name, src, tgt, theta, eps, order="radix", fused=False):
+def workload_config(name, src, tgt, theta, eps, order="radix", fused=False, shards=1):
     m = int(src.shape[0] if tgt is None else tgt.shape[0])
-    return {"workload": name, "n_sources": int(src.shape[0]),
+    extra = {} if shards == 1 else {
+        "parallelism": f"targets split over {shards} ranks: sources replicated, each rank "
+                       "builds the whole tree and walks 1/N of the target groups; rows "
+                       "combined by an all-reduce of zero-filled buffers"}
+    return {"workload": name, "n_sources": int(src.shape[0]), **extra,
             "n_targets": m,
             "theta": theta, "eps": eps, "opening": f"warp vote, groups of {walk_group(m)}",
             "walk": "fused" if fused else "producer/consumer warp pairs",
@@ -379,64 +409,102 @@ def workload_config(name, src, tgt, theta, eps, order="radix", fused=False):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, rank, local_rank, world):
-    import numpy as np
+def shard_groups(ngroups: int, shards: int, shard: int) -> tuple[int, int]:
+    """The walk groups [G s / S, G (s + 1) / S) that shard s of S walks
+    (integer division; the library's BH_OPT_SHARDS rule)."""
+    return ngroups * shard // shards, ngroups * (shard + 1) // shards
+
+
+def gather_rows(out, world: int) -> None:
+    """Give every rank all result rows, in caller order.  Each rank's buffer
+    holds the rows of the groups its shard walked and +0.0 in every other
+    row, so a sum over ranks reproduces each row exactly (x + 0 = x in IEEE
+    arithmetic, whatever order the collective adds in)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(out, op=dist.ReduceOp.SUM)
+
+
+def gpu_stage_medians(stage_times: list[dict]) -> dict:
+    """Per-stage medians (ms) of the GPU stage times of the timed steps
+    (bh_get_stage_times, one dict per step)."""
+    return {k: statistics.median(s[k] for s in stage_times) for k in stage_times[0]}
+
+
+def stage_hbm(stages_ms: dict, nbytes: dict, peak_gbs: float) -> dict:
+    gbs = {k: nbytes[k] / (stages_ms[k] * 1e-3) / 1e9
+           for k in nbytes if stages_ms.get(k, 0) > 0}
+    return {"unit": "GB/s", "peak": peak_gbs,
+            "achieved": {k: round(v, 1) for k, v in gbs.items()},
+            "frac": {k: round(v / peak_gbs, 3) for k, v in gbs.items()}}
+
+
+def measure_workload(name, args, device, rank, local_rank, world, split: bool,
+                     e2e_steps: int):
+    """Time one workload: the headline loop (library defaults, so a
+    repeated call replays its captured graph), the per-stage loop, and the
+    end-to-end loop from pinned host memory.  With split (N > 1) every rank
+    builds the whole tree from the replicated sources, walks its shard of the
+    target groups into a zeroed buffer, and the rows are combined over the
+    ranks (gather_rows) inside every timed step."""
     import torch
 
     import barnes_hut_body_gb300 as B
     import workloads as W
 
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    dist_init(world, "nccl")
-    src, tgt, G, eps, theta = W.make(args.workload)
+    src, tgt, G, eps, theta = W.make(name)
     theta = args.theta if args.theta is not None else theta
     m = src.shape[0] if tgt is None else tgt.shape[0]
     d_src = torch.from_numpy(src).to(device)
     d_tgt = None if tgt is None else torch.from_numpy(tgt).to(device)
-    d_out = torch.empty((m, 4), dtype=torch.float32, device=device)
+    d_out = torch.zeros((m, 4), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
     order = B.BH_ORDER_TREE if args.order == "tree" else B.BH_ORDER_RADIX
-    bh = B.BarnesHut(theta=theta, G=G, eps=eps, device=local_rank, timing=1, order=order,
-                     pipeline=0 if args.fused_walk else 1)
-    for _ in range(max(args.warmup, 3)):
-        bh.compute(d_src, d_tgt, d_out)
-    rc = bh.status()
-    if rc != 0:
-        raise RuntimeError(f"warm-up failed: {B.bh_last_error(bh.ctx)}")
-    useful = B.bh_count_interactions(bh.ctx)
-    torch.cuda.synchronize(device)
+    opts = dict(theta=theta, G=G, eps=eps, device=local_rank, timing=1, order=order,
+                pipeline=0 if args.fused_walk else 1)
+    if split:
+        opts.update(shards=world, shard=rank)
+    bh = B.BarnesHut(**opts)
 
+    def step(out=d_out, s_in=d_src, t_in=d_tgt):
+        if split:
+            out.zero_()
+        bh.compute(s_in, t_in, out)
+        if split:
+            gather_rows(out, world)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if bh.status() != 0:
+        raise RuntimeError(f"warm-up failed: {B.bh_last_error(bh.ctx)}")
+    useful = B.bh_count_interactions(bh.ctx)          # all targets, every shard
+    torch.cuda.synchronize(device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
 
     # breakdown: the step with per-stage CUDA events (launched kernel by
     # kernel, since events cannot be recorded inside the captured graph)
-    stage_ms = []
-    executed = []
+    stage_list, executed = [], []
     barrier(world, device)
     torch.cuda.synchronize(device)
     for k in range(args.steps):
         flush.fill_(float(k))                    # evict L2 (untimed)
         ev[k][0].record(stream)
-        bh.compute(d_src, d_tgt, d_out)
+        step()
         ev[k][1].record(stream)
-        stage_ms.append(B.bh_get_stage_times(bh.ctx))   # waits for the step
+        stage_list.append(B.bh_get_stage_times(bh.ctx))   # waits for the step
         executed.append(B.bh_get_counters(bh.ctx)[0])
     torch.cuda.synchronize(device)
-    rc = bh.status()
-    if rc != 0:
+    if bh.status() != 0:
         raise RuntimeError(f"timed steps failed: {B.bh_last_error(bh.ctx)}")
-    eager_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev),
-                              world, device)
+    eager_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
 
-    # headline: the library's defaults (no stage events), so the repeated
-    # call replays its captured graph -- every kernel of the step, every time
+    # headline: the library's defaults (no stage events)
     B.bh_set_option(bh.ctx, B.BH_OPT_TIMING, 0)
     for _ in range(3):
-        bh.compute(d_src, d_tgt, d_out)
+        step()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     barrier(world, device)
     torch.cuda.synchronize(device)
@@ -446,103 +514,154 @@ def run_ours(args, rank, local_rank, world):
     for k in range(args.steps):
         flush.fill_(float(k))
         ev[k][0].record(stream)
-        bh.compute(d_src, d_tgt, d_out)
+        step()
         ev[k][1].record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - wall0
     barrier(world, device)
     clocks = sampler.stop() if sampler else None
-    rc = bh.status()
-    if rc != 0:
+    if bh.status() != 0:
         raise RuntimeError(f"timed steps failed: {B.bh_last_error(bh.ctx)}")
     ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, device)
-    total_useful = sum_over_ranks(useful, world, device)
-    value = total_useful / (ms / 1e3)
+    # one problem split over the ranks: its useful terms; replicas: the sum
+    total_useful = useful if split else sum_over_ranks(useful, world, device)
 
-    # end to end through the host-buffer entry point (pinned memory), with
-    # the library's defaults (no per-stage events, so repeated calls replay
-    # the captured graph)
+    # end to end from pinned host memory, with the library's defaults
     h_src = torch.from_numpy(src).pin_memory()
     h_tgt = None if tgt is None else torch.from_numpy(tgt).pin_memory()
     h_out = torch.empty((m, 4), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        if not split:
+            B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
+            return
+        d_src.copy_(h_src, non_blocking=True)
+        if h_tgt is not None:
+            d_tgt.copy_(h_tgt, non_blocking=True)
+        step()
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+
     for _ in range(3):                   # the second identical call captures the graph
-        B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
+        e2e_step()
     barrier(world, device)
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        B.bh_compute_host(bh.ctx, h_src, h_tgt, h_out, stream.cuda_stream)
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / args.e2e_steps, world, device)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, device)
     h2d = 16 * (src.shape[0] + (0 if tgt is None else tgt.shape[0]))
-    d2h = 16 * m
 
-    stages = {k: statistics.median([s[k] for s in stage_ms]) for k in stage_ms[0]}
+    stages = gpu_stage_medians(stage_list)
     walk_ms = stages["traverse"]
     nodes = int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_NODE_COUNT)[0])
-    sbytes = stage_bytes(src.shape[0], m, nodes, tgt is None, args.order)
-    traffic = WALK_TRAFFIC_BYTES if (not args.fused_walk and args.order == "radix"
-                                     and args.workload == "lattice1m_shuffled") else None
     hbm_peak = measured_hbm_gbs()
-    stage_gbs = {k: sbytes[k] / (stages[k] * 1e-3) / 1e9 for k in sbytes if stages.get(k, 0) > 0}
     exec_terms = statistics.median(executed)
     props = torch.cuda.get_device_properties(device)
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     achieved = exec_terms * FLOPS_PER_TERM / (walk_ms / 1e3) / 1e12
+    traffic = WALK_TRAFFIC_BYTES if (not args.fused_walk and args.order == "radix"
+                                     and name == "lattice1m_shuffled" and not split) else None
+    res = {
+        "ms_per_step": ms, "eager_ms_per_step": eager_ms,
+        "stage_ms": {k: round(v, 4) for k, v in stages.items()},
+        "useful_per_step": useful, "executed_per_step": exec_terms, "nodes": nodes,
+        "value": total_useful / (ms / 1e3),
+        "stage_hbm": stage_hbm(stages, stage_bytes(src.shape[0], m, nodes, tgt is None,
+                                                   args.order), hbm_peak),
+        "stage_hbm_kernel_bytes": stage_hbm(stages, kernel_bytes(src.shape[0], m, nodes),
+                                            hbm_peak),
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "walk_kernel<2,vote>" if args.fused_walk
+                               else "walk_ws_kernel<2,vote>",
+                     "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz"},
+        "e2e": {"value": total_useful / (e2e_ms / 1e3), "unit": "interactions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 16 * m,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": kernels_per_step(args.order, src.shape[0],
+                                         None if tgt is None else tgt.shape[0],
+                                         props.multi_processor_count,
+                                         scheduled=not split) * args.steps,
+        "clocks": clocks, "wall_s_timed": wall,
+        "config": workload_config(name, src, tgt, theta, eps, args.order, args.fused_walk,
+                                  shards=world if split else 1),
+    }
+    return res, bh, stream, (src, tgt, G, eps, theta)
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    import barnes_hut_body_gb300 as B
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    split = world > 1 and args.split == "targets"
+    res, bh, stream, (src, tgt, G, eps, theta) = measure_workload(
+        args.workload, args, device, rank, local_rank, world, split, args.e2e_steps)
     probe = measured_fp32_tflops(bh.ctx, stream)
+    bh.close()
     peak_meas = max(probe.values())
-    launches = kernels_per_step(args.order, src.shape[0], None if tgt is None else tgt.shape[0],
-                                props.multi_processor_count) * args.steps
+    res["roofline"].update(peak_measured=peak_meas,
+                           frac_measured=res["roofline"]["achieved"] / peak_meas,
+                           probe_tflops=probe)
+    also = {}
+    for name in [a for a in args.also.split(",") if a and a != "none" and a != args.workload]:
+        r, b2, _, _ = measure_workload(name, args, device, rank, local_rank, world, split,
+                                       min(args.e2e_steps, 3))
+        b2.close()
+        r["roofline"].update(frac_measured=r["roofline"]["achieved"] / peak_meas)
+        also[name] = {k: r[k] for k in ("config", "ms_per_step", "eager_ms_per_step", "value",
+                                        "stage_ms", "useful_per_step", "executed_per_step",
+                                        "nodes", "stage_hbm", "roofline", "e2e", "clocks",
+                                        "gpu_launches")}
 
     if rank == 0:
+        m = src.shape[0] if tgt is None else tgt.shape[0]
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             import oracle as O
             s, u = cpu_oracle_step(src, tgt, G, eps, theta, args.cpu_sample)
             cores = O.num_threads()
-            stages = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
+            cpu_stages = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
             O.set_threads(1)
-            stages1 = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
+            cpu_stages1 = cpu_oracle_stages(src, tgt, G, eps, theta, args.cpu_sample)
             O.set_threads(cores)
             cpu = {"value": u / s, "unit": "interactions/s", "cores": cores,
                    "kind": "oracle",
                    "sample": f"build over all {src.shape[0]} sources + per-target walk of "
                              f"{min(args.cpu_sample, m)} sampled targets, walk time scaled to {m}",
-                   "stages_s": stages,
-                   "one_core": {"value": u / stages1["step"], "cores": 1, "stages_s": stages1},
+                   "stages_s": cpu_stages,
+                   "one_core": {"value": u / cpu_stages1["step"], "cores": 1,
+                                "stages_s": cpu_stages1},
                    "stages_note": "each stage timed alone over the whole problem; walk of "
                                   f"{min(args.cpu_sample, m)} and fp64 direct sum of "
                                   f"{min(256, m)} sampled targets, scaled to {m} "
                                   "(direct: extrapolated)"}
         line = {
-            "metric": "useful_interactions_per_s", "value": value, "unit": "interactions/s",
-            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "metric": "useful_interactions_per_s", "value": res["value"],
+            "unit": "interactions/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "strong" if split else "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(args.workload, src, tgt, theta, eps, args.order,
-                                      args.fused_walk),
-            "eager_ms_per_step": eager_ms,
-            "stage_ms": {k: round(v, 4) for k, v in stages.items()},
-            "useful_per_step": useful, "executed_per_step": exec_terms, "nodes": nodes,
-            "stage_hbm": {"unit": "GB/s", "peak": hbm_peak,
-                          "achieved": {k: round(v, 1) for k, v in stage_gbs.items()},
-                          "frac": {k: round(v / hbm_peak, 3) for k, v in stage_gbs.items()}},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": traffic,
-                         "kernel": "walk_kernel<2,vote>" if args.fused_walk
-                                   else "walk_ws_kernel<2,vote>",
-                         "peak_note": "fp32 FMA: SMs x 128 lanes x 2 x 2070 MHz",
-                         "peak_measured": peak_meas, "frac_measured": achieved / peak_meas,
-                         "probe_tflops": probe},
-            "e2e": {"value": total_useful / (e2e_ms / 1e3), "unit": "interactions/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": launches,
-            "clocks": clocks,
-            "wall_s_timed": wall,
+            "config": res["config"],
+            **{k: res[k] for k in ("eager_ms_per_step", "stage_ms", "useful_per_step",
+                                   "executed_per_step", "nodes", "stage_hbm",
+                                   "stage_hbm_kernel_bytes", "roofline", "e2e",
+                                   "gpu_launches", "clocks", "wall_s_timed")},
+            "stage_bytes_note": "stage_hbm: the algorithmic bytes per unit (bbox 16/particle, "
+                                "keys 24, sort 24 per pass and element, reorder 36, build "
+                                "8/key + 32/node, CoM 16/particle + 32/node); "
+                                "stage_hbm_kernel_bytes: what the build and CoM kernels "
+                                "read and write by design (keys read twice + 25/node; "
+                                "16/particle + 69/node)",
         }
+        if also:
+            line["also"] = also
         if cpu:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
-    bh.close()
     return 0
 
 
@@ -820,8 +939,11 @@ def run_neighbors(args, rank, local_rank, world):
 
 def main():
     args = parse()
+    default_workload = args.workload is None
     if args.workload is None:
         args.workload = "surface2e20" if args.stochastic else "lattice1m_shuffled"
+    if args.also is None:
+        args.also = "galaxy5m" if default_workload else "none"
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)

@@ -87,3 +87,49 @@ def test_energy_drift_small_with_tree_forces():
     p, v, _, _ = _run(pm, vel, 0.5, 1.0, eps, 1e-3, 100)
     e1 = energy(p, v)
     assert abs(e1 - e0) < 1e-3 * abs(e0)
+
+
+def test_tree_force_trajectory_within_force_error_budget():
+    """theta = 0.5 against the oracle's fp64 leapfrog with exact forces, 2048
+    Plummer particles, 20 steps of 1e-3 (T = 0.02, about half a central
+    dynamical time).
+
+    Budget, derived from the force error: a force error |da| <= D applied
+    over [0, T] moves a leapfrog trajectory by at most (T^2 / 2) D g and
+    changes its velocity by at most T D g, where g = cosh(w T) bounds the
+    growth of a deviation under tidal fields of rate w^2.  Here w^2 <= G M /
+    a^3 = 1000 (Plummer centre; the softened pair tide G m / eps^3 = 488 is
+    smaller), so g <= cosh(0.64) < 1.25; the test uses g = 2.  D is the
+    largest Barnes-Hut force error of the GPU's opening rule (the oracle's
+    group walk, groups of 32, vote) against the direct sum, taken at the
+    first and the last positions of the exact trajectory.  Rounding adds the
+    theta = 0 test's allowance."""
+    n, G, eps, dt, nsteps, theta = 2048, 1.0, 1e-2, 1e-3, 20, 0.5
+    pm = W.plummer(n, seed=54)
+    g = W.rng(54)
+    r = np.linalg.norm(pm[:, :3].astype(np.float64), axis=1)
+    vesc = np.sqrt(2.0 / np.sqrt(r * r + 0.01))
+    vel = (g.normal(size=(n, 3)) * (0.35 * vesc)[:, None] / np.sqrt(3)).astype(np.float32)
+    p_gpu, v_gpu, _, _ = _run(pm, vel, theta, G, eps, dt, nsteps)
+    p_ref, v_ref = O.leapfrog(pm, vel, G, eps, dt, nsteps)
+
+    def force_error(p):
+        p32 = np.ascontiguousarray(p, np.float32)
+        o = O.OracleBH(p32, theta=theta, G=G, eps=eps, leaf_cap=16)
+        bh, rows, _ = o.bh_group(group=32, mode=0)
+        exact = O.direct(p32, None, G, eps)[rows]
+        return np.linalg.norm(bh[:, :3] - exact[:, :3], axis=1).max()
+
+    T = dt * nsteps
+    D = max(force_error(pm), force_error(p_ref))
+    growth = 2.0
+    dx = np.linalg.norm(p_gpu[:, :3] - p_ref[:, :3], axis=1)
+    dv = np.linalg.norm(v_gpu[:, :3] - v_ref[:, :3], axis=1)
+    x_tol = 0.5 * T * T * D * growth + 2e-5 * np.abs(p_ref[:, :3]).max()
+    v_tol = T * D * growth + 2e-4 * np.abs(v_ref).max()
+    assert dx.max() <= x_tol, (dx.max(), x_tol)
+    assert dv.max() <= v_tol, (dv.max(), v_tol)
+    # the budget is well inside the motion it checks
+    moved = np.linalg.norm(p_ref[:, :3] - pm[:, :3].astype(np.float64), axis=1)
+    assert x_tol < 0.2 * np.median(moved), (x_tol, np.median(moved))
+    np.testing.assert_array_equal(p_gpu[:, 3], pm[:, 3])

@@ -133,3 +133,25 @@ def test_tree_order_pool_overflow_is_reported_and_recovers(B):
     assert rc == 0
     np.testing.assert_array_equal(got, ref)
     bh.close()
+
+
+@pytest.mark.parametrize("name", ["lattice1m_shuffled", "galaxy5m"])
+def test_tree_order_full_size(B, name):
+    """The two workloads bench.py --order tree times, at full size (1M
+    shuffled lattice, 5M galaxy pair): the permutation equals the oracle's
+    stable sort, the sorted keys and every tree node equal the oracle's, and
+    the results equal the radix path's bit for bit."""
+    src, tgt, G, eps, theta = W.make(name)
+    n = src.shape[0]
+    bh_t, b, rc_t = H.gpu_bh(src, theta=theta, G=G, eps=eps, order=B.BH_ORDER_TREE)
+    assert rc_t == 0
+    o = O.OracleBH(src, theta=theta, G=G, eps=eps, leaf_cap=16)
+    np.testing.assert_array_equal(B.bh_debug_export(bh_t.ctx, B.BH_EXPORT_PERM, n), o.perm)
+    np.testing.assert_array_equal(B.bh_debug_export(bh_t.ctx, B.BH_EXPORT_KEYS, n), o.skeys)
+    nn = int(B.bh_debug_export(bh_t.ctx, B.BH_EXPORT_NODE_COUNT)[0])
+    H.assert_tree_equal(B.bh_debug_export(bh_t.ctx, B.BH_EXPORT_NODES, nn), o.tree)
+    bh_t.close()
+    bh_r, a, rc_r = H.gpu_bh(src, theta=theta, G=G, eps=eps, order=B.BH_ORDER_RADIX)
+    assert rc_r == 0
+    np.testing.assert_array_equal(a, b)
+    bh_r.close()
