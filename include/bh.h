@@ -233,11 +233,14 @@ typedef struct bh_ctx bh_ctx;
  * Create a context on CUDA device `device` with scratch for up to
  * `max_sources` particles and `max_targets` separate targets (either may be
  * 0; buffers grow on demand).  Defaults: theta 0.5, G 1, eps 0, options as
- * listed above.  *out is set to NULL on failure.
+ * listed above.  *out is set to NULL on failure.  The GASPHiA page's code
+ * allocates its device arrays in a class constructor (section "计算核函数",
+ * the d_* arrays its kernels take); the context is that holder, in C form.
  */
 int bh_create(bh_ctx **out, int device, size_t max_sources, size_t max_targets);
 
-/* Destroy a context and free its scratch.  NULL is accepted. */
+/* Destroy a context and free its scratch.  NULL is accepted.  No
+ * counterpart in the pages (they free nothing explicitly). */
 int bh_destroy(bh_ctx *c);
 
 /*
@@ -249,10 +252,16 @@ int bh_destroy(bh_ctx *c);
  */
 int bh_set_params(bh_ctx *c, float theta, float G, float eps);
 
-/* Set an option (BH_OPT_*).  BH_EINVAL for an unknown key or bad value. */
+/* Set an option (BH_OPT_*).  BH_EINVAL for an unknown key or bad value.
+ * Each option cites its passage above where the pages have one (key width
+ * and spatial sort: the tree page's section "实现步骤"; the opening rule and
+ * vote: the GASPHiA page's section "性能瓶颈分析"; the tree order: its
+ * section "排序算法"); the rest (timing, graph replay, group size, pipeline,
+ * shards, schedule) are this library's and have no counterpart. */
 int bh_set_option(bh_ctx *c, int key, long long value);
 
-/* Set a debug knob (BH_DBG_*); for tests of the failure paths. */
+/* Set a debug knob (BH_DBG_*); for tests of the failure paths.  No
+ * counterpart in the pages. */
 int bh_set_debug(bh_ctx *c, int key, long long value);
 
 /*
@@ -352,6 +361,9 @@ int bh_leapfrog(bh_ctx *c, float *pos_mass, float *vel, size_t n,
 /*
  * Synchronise `stream`, then return and clear the device status word
  * (BH_OK, BH_EINVAL for non-finite input, BH_ETIMEOUT, BH_ETREE_OVERFLOW).
+ * The GASPHiA page checks every CUDA call and stops the program on an error
+ * (its CUDA_CHECK macro, section "计算核函数"); here kernels record errors
+ * in a status word instead, so the host learns of them without a fatal exit.
  */
 int bh_sync_status(bh_ctx *c, void *stream);
 
@@ -407,6 +419,9 @@ int bh_fp32_probe(bh_ctx *c, int packed, int iters, double *flops, void *stream)
  * Per-stage milliseconds of the last bh_compute made with BH_OPT_TIMING on
  * (indices BH_STAGE_*; a stage that did not run reads 0).  Synchronises on
  * the last recorded event.  n = number of floats at ms (<= BH_NUM_STAGES).
+ * The stages are the GASPHiA page's timed kernels (section "性能测试与对比":
+ * reset, bounding box, build, centre of mass, gravity), with the sort and
+ * reorder of the tree page's section "实现步骤" timed on their own.
  */
 int bh_get_stage_times(bh_ctx *c, float *ms, int n);
 
@@ -417,6 +432,12 @@ int bh_get_stage_times(bh_ctx *c, float *ms, int n);
  * per surviving step, the cell's children (or particles) and the cell);
  * `groups` = number of target groups walked.  After bh_neighbors,
  * `executed` = pair tests of its counting walk.
+ * The "useful" count -- the terms of the per-target rule, the textbook
+ * Barnes-Hut walk the GASPHiA page's section "性能瓶颈分析" starts from --
+ * is not a by-product of the group walk: the group accepts a cell only when
+ * all its targets do, so its terms are a superset and which of them a lone
+ * target would have needed is never decided.  bh_count_interactions runs
+ * that per-target walk separately (counting only, outside the step).
  */
 int bh_get_counters(bh_ctx *c, unsigned long long *executed,
                     unsigned long long *groups);
@@ -438,11 +459,14 @@ int bh_count_interactions(bh_ctx *c, unsigned int *counts,
 /*
  * Copy internal state of the last bh_compute to host memory (synchronises
  * the device).  `what` is a BH_EXPORT_* key; `bytes` is the size of
- * host_dst, which must hold the whole item (BH_EINVAL otherwise).
+ * host_dst, which must hold the whole item (BH_EINVAL otherwise).  For the
+ * bit-exact parity checks of keys, permutation and tree; no counterpart in
+ * the pages.
  */
 int bh_debug_export(bh_ctx *c, int what, void *host_dst, size_t bytes);
 
-/* Message for the last failed call on this context ("" if none). */
+/* Message for the last failed call on this context ("" if none).  No
+ * counterpart in the pages. */
 const char *bh_last_error(const bh_ctx *c);
 
 #ifdef __cplusplus
