@@ -149,8 +149,8 @@ void free_sources(bh_ctx *c) {
   for (int k = 0; k < 2; ++k) { free_dev(c->sort.keys[k]); free_dev(c->sort.idx[k]); }
   free_dev(c->spm);
   free_dev(c->build.topo); free_dev(c->build.parent); free_dev(c->build.level);
-  free_dev(c->build.arrive); free_dev(c->build.msum); free_dev(c->build.rec);
-  free_dev(c->build.tile_counts);
+  free_dev(c->build.arrive); free_dev(c->build.pq); free_dev(c->build.rec);
+  free_dev(c->build.tile_counts); free_dev(c->build.tile_q);
   c->cap_n = 0; c->cap_nodes = 0;
 }
 
@@ -225,10 +225,11 @@ int ensure_sources(bh_ctx *c, long long n) {
   ok = ok && alloc_dev(c->build.parent, nodes);
   ok = ok && alloc_dev(c->build.level, nodes);
   ok = ok && alloc_dev(c->build.arrive, nodes);
-  ok = ok && alloc_dev(c->build.msum, nodes);
+  ok = ok && alloc_dev(c->build.pq, 8 * nodes);
   ok = ok && alloc_dev(c->build.rec, nodes);
   long long btiles = (cap + 1 + kBuildTile - 1) / kBuildTile;
   ok = ok && alloc_dev(c->build.tile_counts, btiles * kMaxLevels);
+  ok = ok && alloc_dev(c->build.tile_q, 4 * btiles);
   if (!ok) {
     free_sources(c);
     return fail(c, BH_ENOMEM, "source scratch allocation failed");
@@ -347,7 +348,7 @@ cudaError_t enqueue_step(bh_ctx *c, const float4 *pm, long long N,
   if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->bits, c->sort, c->spm, 0, 3, &fb, s);
   else record(c, 3, s);
   record(c, 4, s);
-  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
+  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], c->spm, N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
   record(c, 5, s);
   if (e == cudaSuccess) e = launch_com(c->spm, c->sort.keys[fb], N, c->bits, c->theta, c->build, c->ctrl, s);
   record(c, 6, s);
@@ -850,7 +851,7 @@ int bh_neighbors(bh_ctx *c, const float *pos_mass, const float *h, size_t n,
   if (e == cudaSuccess) e = launch_bbox(pm, N, c->partials, c->bbox_blocks, c->ctrl, 0, c->bits, true, s);
   if (e == cudaSuccess) e = launch_keys(pm, N, c->sort.keys[0], c->ctrl, 0, c->bits, s);
   if (e == cudaSuccess) e = enqueue_order(c, pm, N, c->bits, c->sort, c->spm, 0, -1, &fb, s);
-  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
+  if (e == cudaSuccess) e = launch_build(c->sort.keys[fb], c->spm, N, c->bits, c->leaf_cap, c->build, c->ctrl, s);
   NbArgs a;
   a.spm = c->spm;
   a.sh = c->nb_h;

@@ -135,6 +135,9 @@ struct PersistCtrl {
   float4 cube[2];            // (lo_x, lo_y, lo_z, L): sources, targets
   float scale[2];            // 2^bits / L, fp32 IEEE division
   float pad2[2];
+  int qexp[2][2];            // fixed-point moments: 2^k_m scales a mass,
+                             // 2^k_x a mass x (coordinate - lo); chosen so
+                             // that n * max|m| fits in 2^62 (0, 0: no mass)
 };
 
 struct DevCtrl {
@@ -205,16 +208,21 @@ struct BuildBufs {
   int *parent;
   unsigned char *level;
   int *arrive;
-  float4 *msum;          // (sum m x, sum m y, sum m z, sum m)
+  long long *pq;         // per node 8 x int64: the fixed-point moment prefix
+                         // (m, m x, m y, m z) at the node's first particle,
+                         // then at one past its last, each relative to the
+                         // start of the build tile holding that position
   NodeRec *rec;
   unsigned int *tile_counts;   // [level][tile]
+  long long *tile_q;           // [tile][4]: the tile's moment sums, then the
+                               // prefix before the tile
   long long cap_nodes;
   int cap_tiles;
 };
 
-cudaError_t launch_build(const unsigned long long *skeys, long long n, int bits,
-                         int leaf_cap, BuildBufs &b, DevCtrl *ctrl,
-                         cudaStream_t s);
+cudaError_t launch_build(const unsigned long long *skeys, const float4 *spm,
+                         long long n, int bits, int leaf_cap, BuildBufs &b,
+                         DevCtrl *ctrl, cudaStream_t s);
 cudaError_t launch_com(const float4 *spm, const unsigned long long *skeys,
                        long long n, int bits, float theta, BuildBufs &b,
                        DevCtrl *ctrl, cudaStream_t s);

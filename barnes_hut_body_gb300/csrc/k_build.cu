@@ -27,10 +27,20 @@
 // octant order, so the walk reads a node's children as one coalesced block.
 //
 // Centre of mass (GASPHiA page, section "计算核函数": computeCenterOfMass):
-// every leaf sums its particles; a child that finishes bumps its parent's
-// arrival counter and the child that arrives last sums the parent's children
-// (in index order, so the result is deterministic) and carries on upward.
-// No thread ever waits for another.
+// a cell's mass and mass moments are sums over a contiguous range of the
+// sorted particles, so they are differences of two prefix sums.  The prefix
+// sums are kept exactly: every particle's mass m and moments m (x - lo)
+// (per axis, lo = the cube's corner) are scaled by powers of two chosen from
+// the largest |m|, the cube and n, and rounded to 64-bit integers (the
+// product m (x - lo) is formed exactly from the two 24-bit mantissas, so the
+// only rounding is the final one, to half a unit of 2^-k), which makes the
+// sums exact and independent of the order they are formed in.  The write
+// pass forms them for its tile: the thread at a cell's first key records the
+// prefix there and the thread one past its last key the prefix at the end,
+// both relative to their tile, and the tile's sums go out; one block turns
+// the tiles' sums into tile prefixes.  Every node then takes mass =
+// difference of the mass prefixes and com = lo + (difference of the moment
+// prefixes) / mass, on its own: no pass waits for its children.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,15 +63,20 @@ __device__ __forceinline__ int lcp_levels(unsigned long long a,
 }
 
 constexpr int kHalo = kMaxLeafCap + 1;
+constexpr int kLamLen = kBuildTile + kHalo + 1;
 
 struct TileGeom {
   // keys of positions [tb - B - 1, tb + kBuildTile + B]
   unsigned long long k[kBuildTile + 2 * kHalo + 2];
-  signed char lam[kBuildTile + kHalo + 1];   // lcp(key_i, key_{i+B})
+  signed char lam[2][kLamLen];               // lcp(key_i, key_{i+B}), and
+                                             // window maxima built from it
   signed char D[kBuildTile + 1];             // deepest over-full level at j
 };
 
 // Fill the tile geometry for positions j in [tb, tb + kBuildTile).
+// D_j = max of lam over the B + 1 windows [i, i + B] that contain j; the
+// maximum over B + 1 consecutive values comes from a sparse table: the
+// maxima of runs of 2^s values by doubling, then two overlapping runs.
 __device__ void load_geom(TileGeom &g, const unsigned long long *skeys,
                           long long n, long long tb, int B, int bits) {
   const long long k0 = tb - B - 1;
@@ -72,21 +87,30 @@ __device__ void load_geom(TileGeom &g, const unsigned long long *skeys,
   }
   __syncthreads();
   // lam[y] for i = k0 + y, y in [0, kBuildTile + B + 1)
-  for (int y = threadIdx.x; y < kBuildTile + B + 1; y += blockDim.x) {
+  const int nl = kBuildTile + B + 1;
+  for (int y = threadIdx.x; y < nl; y += blockDim.x) {
     long long i = k0 + y;
     signed char v = -1;
     if (i >= 0 && i + B <= n - 1) v = (signed char)lcp_levels(g.k[y], g.k[y + B], bits);
-    g.lam[y] = v;
+    g.lam[0][y] = v;
   }
   __syncthreads();
-  // D[z] for j = tb - 1 + z: max lam over i in [j - B, j]  (lam index i - k0)
-  for (int z = threadIdx.x; z < kBuildTile + 1; z += blockDim.x) {
-    int m = -1;
-    for (int q = 0; q <= B; ++q) {
-      int v = g.lam[z + q];            // i = j - B + q  ->  y = z + q
-      m = v > m ? v : m;
+  // runs of p = 2^s values: run[y] = max lam[y .. y + p - 1]
+  const int W = B + 1;
+  int p = 1, cur = 0;
+  while (2 * p <= W) {
+    for (int y = threadIdx.x; y + p < nl; y += blockDim.x) {
+      const signed char a = g.lam[cur][y], b = g.lam[cur][y + p];
+      g.lam[cur ^ 1][y] = a > b ? a : b;
     }
-    g.D[z] = (signed char)m;
+    __syncthreads();
+    cur ^= 1;
+    p *= 2;
+  }
+  // D[z] for j = tb - 1 + z: windows i in [j - B, j] -> lam index z .. z + B
+  for (int z = threadIdx.x; z < kBuildTile + 1; z += blockDim.x) {
+    const signed char a = g.lam[cur][z], b = g.lam[cur][z + W - p];
+    g.D[z] = a > b ? a : b;
   }
   __syncthreads();
 }
@@ -120,6 +144,100 @@ __device__ __forceinline__ void position_facts(const TileGeom &g, long long n,
 }
 
 // ---------------------------------------------------------------------------
+// fixed-point moments of one particle: (m, m dx, m dy, m dz) scaled by
+// 2^k_m and 2^k_x, d = coordinate - lo rounded once in fp32
+// ---------------------------------------------------------------------------
+struct Q4 {
+  long long m, x, y, z;
+};
+
+// A float as mantissa 2^(e - 150): the 24-bit mantissa with its hidden bit
+// (none for a subnormal, whose e is then 1) and the biased exponent e.
+__device__ __forceinline__ unsigned split_float(float v, int &e) {
+  const unsigned u = __float_as_uint(v);
+  e = (int)((u >> 23) & 0xffu);
+  const unsigned mant = u & 0x7fffffu;
+  if (e) return mant | 0x800000u;
+  e = 1;
+  return mant;
+}
+
+// P 2^s rounded to the nearest integer (ties away from zero); the result
+// must be below 2^63.  ((P >> (t - 1)) + 1) >> 1 is (P + 2^(t-1)) >> t
+// without the overflow.
+__device__ __forceinline__ unsigned long long shift_round(unsigned long long P, int s) {
+  const int sl = s < 0 ? 0 : (s > 63 ? 63 : s);
+  const int t = -s < 1 ? 1 : (-s > 64 ? 64 : -s);
+  const unsigned long long left = P << sl;
+  const unsigned long long right = ((P >> (t - 1)) + 1ull) >> 1;
+  return s >= 0 ? left : right;
+}
+
+// Moments of one particle, exact up to the final rounding to an integer:
+// m 2^k_m, and m d 2^k_x per axis with d = coordinate - lo (rounded once in
+// fp32, >= 0), the product m d formed exactly as (M D) 2^(e_m + e_d - 300)
+// from the two mantissas.
+__device__ __forceinline__ Q4 moments(float4 p, float4 cube, int km, int kx) {
+  int em;
+  const unsigned M = split_float(p.w, em);
+  const bool neg = __float_as_uint(p.w) >> 31;
+  const float d[3] = {__fsub_rn(p.x, cube.x), __fsub_rn(p.y, cube.y),
+                      __fsub_rn(p.z, cube.z)};
+  long long v[4];
+  v[0] = (long long)shift_round(M, em - 150 + km);
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    int ed;
+    const unsigned D = split_float(d[a], ed);
+    v[1 + a] = (long long)shift_round((unsigned long long)M * D, em + ed - 300 + kx);
+  }
+  Q4 q;
+  q.m = neg ? -v[0] : v[0];
+  q.x = neg ? -v[1] : v[1];
+  q.y = neg ? -v[2] : v[2];
+  q.z = neg ? -v[3] : v[3];
+  return q;
+}
+
+__device__ __forceinline__ void q_add(Q4 &a, const Q4 &b) {
+  a.m += b.m; a.x += b.x; a.y += b.y; a.z += b.z;
+}
+
+__device__ __forceinline__ Q4 q_shfl_xor(const Q4 &a, int o) {
+  Q4 r;
+  r.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  r.x = __shfl_xor_sync(0xffffffffu, a.x, o);
+  r.y = __shfl_xor_sync(0xffffffffu, a.y, o);
+  r.z = __shfl_xor_sync(0xffffffffu, a.z, o);
+  return r;
+}
+
+__device__ __forceinline__ Q4 q_shfl_up(const Q4 &a, int o) {
+  Q4 r;
+  r.m = __shfl_up_sync(0xffffffffu, a.m, o);
+  r.x = __shfl_up_sync(0xffffffffu, a.x, o);
+  r.y = __shfl_up_sync(0xffffffffu, a.y, o);
+  r.z = __shfl_up_sync(0xffffffffu, a.z, o);
+  return r;
+}
+
+// Moments of the kQPer consecutive positions tb + kQPer * threadIdx.x + u of
+// this tile (0 past the last particle); `each` receives them one by one.
+constexpr int kQPer = kBuildTile / kBuildThreads;
+
+__device__ __forceinline__ void thread_moments(const float4 *__restrict__ spm, long long n,
+                                               long long tb, float4 cube, int km, int kx,
+                                               Q4 (&each)[kQPer]) {
+  const long long j0 = tb + (long long)kQPer * threadIdx.x;
+  float4 p[kQPer];
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u)
+    p[u] = (j0 + u < n) ? __ldg(spm + j0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) each[u] = moments(p[u], cube, km, kx);
+}
+
+// ---------------------------------------------------------------------------
 // count pass: per tile, per level, number of cells that start in the tile
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBuildThreads)
@@ -129,8 +247,8 @@ build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
   __shared__ unsigned s_cnt[kMaxLevels];
   const long long tb = (long long)blockIdx.x * kBuildTile;
   if (threadIdx.x < kMaxLevels) s_cnt[threadIdx.x] = 0;
-  load_geom(g, skeys, n, tb, B, bits);
   const int lane = threadIdx.x & 31;
+  load_geom(g, skeys, n, tb, B, bits);       // synchronises the block
   unsigned mine = 0;   // lane l accumulates level l
   for (int it = 0; it < kBuildIters; ++it) {
     long long j = tb + it * kBuildThreads + threadIdx.x;
@@ -155,68 +273,124 @@ build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
 // ---------------------------------------------------------------------------
 constexpr int kScanThreads = 1024;
 
-__global__ void __launch_bounds__(kScanThreads)
-build_scan_kernel(unsigned int *tile_counts, int ntiles, DevCtrl *ctrl) {
-  __shared__ unsigned s_warp[kScanThreads / 32];
-  __shared__ unsigned s_carry;
-  const int l = blockIdx.x;
-  unsigned *row = tile_counts + (long long)l * ntiles;
+// Exclusive scan, in place, of vals[0], vals[stride], ..., vals[(count-1)
+// stride] by one block; returns the total.
+template <typename T>
+__device__ long long block_scan_column(T *vals, long long stride, int count) {
+  __shared__ long long s_warp[kScanThreads / 32];
+  __shared__ long long s_carry;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
-  for (int base = 0; base < ntiles; base += kScanThreads) {
-    int t = base + threadIdx.x;
-    unsigned v = t < ntiles ? row[t] : 0u;
-    unsigned x = v;
+  for (int base = 0; base < count; base += kScanThreads) {
+    const int t = base + threadIdx.x;
+    const long long v = t < count ? (long long)vals[stride * t] : 0;
+    long long x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+      long long y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     if (lane == 31) s_warp[w] = x;
     __syncthreads();
-    unsigned off = 0, tot = 0;
+    long long off = 0, all = 0;
     for (int k = 0; k < kScanThreads / 32; ++k) {
-      unsigned c = s_warp[k];
-      if (k < w) off += c;
-      tot += c;
+      const long long q = s_warp[k];
+      if (k < w) off += q;
+      all += q;
     }
-    unsigned carry = s_carry;
-    if (t < ntiles) row[t] = carry + off + x - v;
+    const long long carry = s_carry;
+    if (t < count) vals[stride * t] = (T)(carry + off + x - v);
     __syncthreads();
-    if (threadIdx.x == 0) s_carry = carry + tot;
+    if (threadIdx.x == 0) s_carry = carry + all;
     __syncthreads();
   }
-  if (threadIdx.x == 0) ctrl->step.level_total[l] = (int)s_carry;
+  return s_carry;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+build_scan_kernel(unsigned int *tile_counts, int ntiles, DevCtrl *ctrl) {
+  const int l = blockIdx.x;
+  const long long tot = block_scan_column(tile_counts + (long long)l * ntiles, 1, ntiles);
+  if (threadIdx.x == 0) ctrl->step.level_total[l] = (int)tot;
 }
 
 // ---------------------------------------------------------------------------
 // write pass
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBuildThreads)
-build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
+// Dynamic shared memory of the write pass: the moment prefix at each of the
+// tile's positions.
+constexpr size_t kWriteDynSmem = sizeof(long long) * 4 * kBuildTile;
+// Writes, per node, the moment prefixes at its first particle and one past
+// its last, each relative to the start of the tile holding that position
+// (the tile's own prefix is added by the centre-of-mass pass), and the
+// tile's moment sums to tile_q[4 tile ..].
+__global__ void __launch_bounds__(kBuildThreads, 4)
+build_write_kernel(const unsigned long long *__restrict__ skeys,
+                   const float4 *__restrict__ spm, long long n,
                    int B, int bits, const unsigned int *__restrict__ tile_off,
-                   int ntiles, DevCtrl *ctrl, int4 *topo, int *parent,
-                   unsigned char *level, int *arrive, long long cap_nodes) {
+                   long long *tile_q, int ntiles, DevCtrl *ctrl, int4 *topo,
+                   int *parent, unsigned char *level, int *arrive, long long *pq,
+                   long long cap_nodes) {
   __shared__ TileGeom g;
   __shared__ unsigned s_cnt[kBuildIters][kLvWarps][kMaxLevels];
   __shared__ long long s_base[kMaxLevels + 1];
+  __shared__ long long s_wq[kBuildThreads / 32][4];
   __shared__ int s_ok;
-  const long long tb = (long long)blockIdx.x * kBuildTile;
+  extern __shared__ longlong2 s_P[];       // [kBuildTile][2]: (m, x), (y, z)
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int tile = blockIdx.x;
+  const long long tb = (long long)tile * kBuildTile;
+  // the tile's moments: local exclusive prefix at positions
+  // tb + kQPer * threadIdx.x + u, and the tile's sums
+  {
+    Q4 each[kQPer];
+    thread_moments(spm, n, tb, ctrl->keep.cube[0], ctrl->keep.qexp[0][0],
+                   ctrl->keep.qexp[0][1], each);
+    Q4 t = each[0];
+#pragma unroll
+    for (int u = 1; u < kQPer; ++u) q_add(t, each[u]);
+    Q4 x = t;                                  // inclusive over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      Q4 y = q_shfl_up(x, o);
+      if (lane >= o) q_add(x, y);
+    }
+    if (lane == 31) {
+      s_wq[w][0] = x.m; s_wq[w][1] = x.x; s_wq[w][2] = x.y; s_wq[w][3] = x.z;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+      long long agg = 0;
+      for (int k = 0; k < kBuildThreads / 32; ++k) agg += s_wq[k][threadIdx.x];
+      tile_q[4LL * tile + threadIdx.x] = agg;
+    }
+    Q4 run;
+    run.m = x.m - t.m; run.x = x.x - t.x; run.y = x.y - t.y; run.z = x.z - t.z;
+    for (int k = 0; k < w; ++k) {
+      run.m += s_wq[k][0]; run.x += s_wq[k][1]; run.y += s_wq[k][2]; run.z += s_wq[k][3];
+    }
+#pragma unroll
+    for (int u = 0; u < kQPer; ++u) {
+      const int pos = kQPer * threadIdx.x + u;
+      s_P[2 * pos] = make_longlong2(run.m, run.x);
+      s_P[2 * pos + 1] = make_longlong2(run.y, run.z);
+      q_add(run, each[u]);
+    }
+  }
   if (threadIdx.x == 0) {
     long long off = 0;
     for (int l = 0; l <= bits; ++l) {
-      s_base[l] = off + tile_off[(long long)l * ntiles + blockIdx.x];
+      s_base[l] = off + tile_off[(long long)l * ntiles + tile];
       off += ctrl->step.level_total[l];
     }
     s_base[bits + 1] = off;
     s_ok = off <= cap_nodes;
-    if (!s_ok && blockIdx.x == 0) set_err(ctrl, kErrOverflow);
+    if (!s_ok && tile == 0) set_err(ctrl, kErrOverflow);
   }
   for (int k = threadIdx.x; k < kBuildIters * kLvWarps * kMaxLevels; k += blockDim.x)
     (&s_cnt[0][0][0])[k] = 0u;
-  load_geom(g, skeys, n, tb, B, bits);
+  load_geom(g, skeys, n, tb, B, bits);       // synchronises the block
   if (!s_ok) return;
   // phase A: per (iteration, warp, level) counts, over the warp's levels only
   int s[kBuildIters], L[kBuildIters], e[kBuildIters], Lp[kBuildIters];
@@ -283,6 +457,9 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
             parent[idx] = par;
             level[idx] = (unsigned char)lv;
             if (fc >= 0) arrive[idx] = 0;
+            longlong2 *d = reinterpret_cast<longlong2 *>(pq + 8 * idx);
+            d[0] = s_P[2 * (j - tb)];
+            d[1] = s_P[2 * (j - tb) + 1];
           }
         }
         if (lv > ej && lv <= Lpj) {            // the cell holding j-1 ends at j
@@ -290,6 +467,9 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
           if (idx >= 0 && idx < cap_nodes) {
             topo[idx].y = (int)j;
             topo[idx].w = (lv < Lpj) ? (int)r_p1 : -1;
+            longlong2 *d = reinterpret_cast<longlong2 *>(pq + 8 * idx + 4);
+            d[0] = s_P[2 * (j - tb)];
+            d[1] = s_P[2 * (j - tb) + 1];
           }
         }
       }
@@ -300,7 +480,15 @@ build_write_kernel(const unsigned long long *__restrict__ skeys, long long n,
 }
 
 // ---------------------------------------------------------------------------
-// centre of mass, bottom up
+// the tiles' moment sums -> exclusive prefixes (one block, exact integers)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kScanThreads)
+tile_prefix_kernel(long long *tile_q, int ntiles) {
+  block_scan_column(tile_q + blockIdx.x, 4, ntiles);    // one column per block
+}
+
+// ---------------------------------------------------------------------------
+// centre of mass: every node on its own, from its two moment prefixes
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ unsigned compact3(unsigned long long key, int axis) {
   unsigned q = 0;
@@ -309,127 +497,104 @@ __device__ __forceinline__ unsigned compact3(unsigned long long key, int axis) {
   return q;
 }
 
-__device__ void finish_node(long long c, float4 sum, int lvl, int link,
-                            int count, bool leaf, float4 cube, float theta,
-                            int bits, const unsigned long long *skeys,
-                            int first_particle, float4 *msum, NodeRec *rec) {
-  msum[c] = sum;
-  NodeRec r;
-  const float w = ldexpf(cube.w, -lvl);            // full cell edge
-  if (sum.w != 0.f) {
-    const float inv = __frcp_rn(sum.w);
-    r.com = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w);
-  } else {                                          // massless: cell centre
-    unsigned long long key = skeys[first_particle];
-    const int sh = bits - lvl;
-    float ctr[3];
-    const float lo[3] = {cube.x, cube.y, cube.z};
-    for (int a = 0; a < 3; ++a) {
-      unsigned cell = compact3(key, a) >> sh;
-      ctr[a] = lo[a] + ((float)cell + 0.5f) * w;
-    }
-    r.com = make_float4(ctr[0], ctr[1], ctr[2], 0.f);
-  }
-  r.ropen2 = __fdiv_rn(__fmul_rn(w, w), __fmul_rn(theta, theta));
-  r.link = link;
-  r.count = count;
-  r.flags = (leaf ? 1 : 0) | (lvl << 8);
-  rec[c] = r;
-}
-
 __global__ void __launch_bounds__(256)
-com_kernel(const float4 *__restrict__ spm, const unsigned long long *skeys,
-           long long n, int bits, float theta, const int4 *__restrict__ topo,
-           const int *__restrict__ parent, const unsigned char *__restrict__ level,
-           int *arrive, float4 *msum, NodeRec *rec, DevCtrl *ctrl,
-           long long cap_nodes) {
+com_kernel(const unsigned long long *__restrict__ skeys, long long n, int bits,
+           float theta, const int4 *__restrict__ topo,
+           const unsigned char *__restrict__ level, const long long *__restrict__ pq,
+           const long long *__restrict__ tile_pre, NodeRec *__restrict__ rec,
+           const DevCtrl *__restrict__ ctrl, long long cap_nodes) {
   long long total = 0;
   for (int l = 0; l <= bits; ++l) total += ctrl->step.level_total[l];
   if (total > cap_nodes) return;
   const float4 cube = ctrl->keep.cube[0];
+  const int km = ctrl->keep.qexp[0][0], kx = ctrl->keep.qexp[0][1];
+  const float th2 = __fmul_rn(theta, theta);
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
        c < total; c += stride) {
-    int4 t = topo[c];
-    if (t.z >= 0) continue;                       // internal: done by a child
-    long long f = t.x < 0 ? 0 : t.x;
-    if (f > n) f = n;
-    long long e = t.y < f ? f : t.y;
-    if (e > n) e = n;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    long long j = f;
-    for (; j + 4 <= e; j += 4) {          // four loads in flight
-      float4 p[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) p[u] = __ldg(spm + j + u);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        s.x = fmaf(p[u].w, p[u].x, s.x);
-        s.y = fmaf(p[u].w, p[u].y, s.y);
-        s.z = fmaf(p[u].w, p[u].z, s.z);
-        s.w += p[u].w;
+    const int4 t = topo[c];
+    const int lvl = level[c];
+    const bool leaf = t.z < 0;
+    long long first = t.x < 0 ? 0 : (t.x > n ? n : t.x);
+    long long end = t.y < first ? first : (t.y > n ? n : t.y);
+    // prefixes at first and end: the node's tile-relative values plus the
+    // prefix before the tile each position falls in
+    const longlong2 *q = reinterpret_cast<const longlong2 *>(pq + 8 * c);
+    const longlong2 *tf = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (first / kBuildTile));
+    const longlong2 *te = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (end / kBuildTile));
+    longlong2 f0 = q[0], f1 = q[1], e0 = q[2], e1 = q[3];
+    const longlong2 tf0 = tf[0], tf1 = tf[1], te0 = te[0], te1 = te[1];
+    f0.x += tf0.x; f0.y += tf0.y; f1.x += tf1.x; f1.y += tf1.y;
+    e0.x += te0.x; e0.y += te0.y; e1.x += te1.x; e1.y += te1.y;
+    const long long dm = e0.x - f0.x;
+    NodeRec r;
+    const float w = ldexpf(cube.w, -lvl);            // full cell edge
+    if (dm != 0) {
+      // com - lo = (sum m d 2^kx) / (sum m 2^km) * 2^(km - kx)
+      const float fm = __ll2float_rn(dm);
+      const int sc = km - kx;
+      r.com = make_float4(
+          __fadd_rn(cube.x, ldexpf(__fdiv_rn(__ll2float_rn(e0.y - f0.y), fm), sc)),
+          __fadd_rn(cube.y, ldexpf(__fdiv_rn(__ll2float_rn(e1.x - f1.x), fm), sc)),
+          __fadd_rn(cube.z, ldexpf(__fdiv_rn(__ll2float_rn(e1.y - f1.y), fm), sc)),
+          ldexpf(fm, -km));
+    } else {                                          // massless: cell centre
+      const unsigned long long key = skeys[first < n ? first : 0];
+      const int sh = bits - lvl;
+      float ctr[3];
+      const float lo[3] = {cube.x, cube.y, cube.z};
+      for (int a = 0; a < 3; ++a) {
+        unsigned cell = compact3(key, a) >> sh;
+        ctr[a] = lo[a] + ((float)cell + 0.5f) * w;
       }
+      r.com = make_float4(ctr[0], ctr[1], ctr[2], 0.f);
     }
-    for (; j < e; ++j) {
-      float4 p = __ldg(spm + j);
-      s.x = fmaf(p.w, p.x, s.x);
-      s.y = fmaf(p.w, p.y, s.y);
-      s.z = fmaf(p.w, p.z, s.z);
-      s.w += p.w;
+    r.ropen2 = __fdiv_rn(__fmul_rn(w, w), th2);
+    if (leaf) {
+      r.link = (int)first;
+      r.count = (int)(end - first);
+    } else {
+      const int nch = t.w - t.z;
+      r.link = t.z;
+      r.count = (nch >= 1 && nch <= 8 && t.w <= total) ? nch : 0;
     }
-    int lvl = level[c];
-    finish_node(c, s, lvl, (int)f, (int)(e - f), true, cube, theta, bits,
-                skeys, (int)(f < n ? f : 0), msum, rec);
-    // climb while this thread is the last child to finish
-    long long node = c;
-    for (int guard = 0; guard <= kMaxLevels; ++guard) {
-      int p = parent[node];
-      if (p < 0 || p >= total) break;
-      __threadfence();
-      int4 tp = topo[p];
-      int nch = tp.w - tp.z;
-      if (tp.z < 0 || nch < 1 || nch > 8 || tp.w > total) break;
-      int old = atomicAdd(arrive + p, 1);
-      if (old != nch - 1) break;
-      __threadfence();
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = tp.z; k < tp.w; ++k) {
-        float4 q = __ldcg(msum + k);
-        a.x += q.x; a.y += q.y; a.z += q.z; a.w += q.w;
-      }
-      int plv = level[p];
-      long long pf = tp.x < 0 ? 0 : (tp.x < n ? tp.x : 0);
-      finish_node(p, a, plv, tp.z, nch, false, cube, theta, bits, skeys,
-                  (int)pf, msum, rec);
-      node = p;
-    }
+    r.flags = (leaf ? 1 : 0) | (lvl << 8);
+    rec[c] = r;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_build(const unsigned long long *skeys, long long n, int bits,
-                         int leaf_cap, BuildBufs &b, DevCtrl *ctrl,
-                         cudaStream_t s) {
+cudaError_t launch_build(const unsigned long long *skeys, const float4 *spm,
+                         long long n, int bits, int leaf_cap, BuildBufs &b,
+                         DevCtrl *ctrl, cudaStream_t s) {
   const long long ntiles = (n + 1 + kBuildTile - 1) / kBuildTile;  // positions 0..n
   if (ntiles > b.cap_tiles) return cudaErrorInvalidValue;
+  // the write pass's moment prefix takes it past the 48 KB default
+  static std::atomic<int> memo[kMaxDevices];
+  const int opted = per_device(memo, [] {
+    return cudaFuncSetAttribute(build_write_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kWriteDynSmem) == cudaSuccess ? 1 : -1;
+  });
+  if (opted < 0) return cudaErrorInvalidValue;
   build_count_kernel<<<(unsigned)ntiles, kBuildThreads, 0, s>>>(
       skeys, n, leaf_cap, bits, b.tile_counts, (int)ntiles);
-  build_scan_kernel<<<bits + 1, kScanThreads, 0, s>>>(b.tile_counts, (int)ntiles,
-                                                      ctrl);
-  build_write_kernel<<<(unsigned)ntiles, kBuildThreads, 0, s>>>(
-      skeys, n, leaf_cap, bits, b.tile_counts, (int)ntiles, ctrl, b.topo,
-      b.parent, b.level, b.arrive, b.cap_nodes);
+  build_scan_kernel<<<bits + 1, kScanThreads, 0, s>>>(b.tile_counts, (int)ntiles, ctrl);
+  build_write_kernel<<<(unsigned)ntiles, kBuildThreads, kWriteDynSmem, s>>>(
+      skeys, spm, n, leaf_cap, bits, b.tile_counts, b.tile_q, (int)ntiles, ctrl,
+      b.topo, b.parent, b.level, b.arrive, b.pq, b.cap_nodes);
+  tile_prefix_kernel<<<4, kScanThreads, 0, s>>>(b.tile_q, (int)ntiles);
   return cudaGetLastError();
 }
 
 cudaError_t launch_com(const float4 *spm, const unsigned long long *skeys,
                        long long n, int bits, float theta, BuildBufs &b,
                        DevCtrl *ctrl, cudaStream_t s) {
+  (void)spm;
   int blocks = sm_count() * 8;
-  com_kernel<<<blocks, 256, 0, s>>>(spm, skeys, n, bits, theta, b.topo,
-                                    b.parent, b.level, b.arrive, b.msum, b.rec,
-                                    ctrl, b.cap_nodes);
+  com_kernel<<<blocks, 256, 0, s>>>(skeys, n, bits, theta, b.topo, b.level, b.pq,
+                                    b.tile_q, b.rec, ctrl, b.cap_nodes);
   return cudaGetLastError();
 }
 

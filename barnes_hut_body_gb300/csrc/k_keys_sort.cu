@@ -47,6 +47,7 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
             DevCtrl *ctrl, int which, int bits, int bump_epoch) {
   float lo0 = INFINITY, lo1 = INFINITY, lo2 = INFINITY;
   float hi0 = -INFINITY, hi1 = -INFINITY, hi2 = -INFINITY;
+  float mm = 0.f;                       // largest |mass|
   bool bad = false;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -58,6 +59,7 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       bad |= !finite4(p[u]);
+      mm = fmaxf(mm, fabsf(p[u].w));
       lo0 = fminf(lo0, p[u].x); hi0 = fmaxf(hi0, p[u].x);
       lo1 = fminf(lo1, p[u].y); hi1 = fmaxf(hi1, p[u].y);
       lo2 = fminf(lo2, p[u].z); hi2 = fmaxf(hi2, p[u].z);
@@ -66,6 +68,7 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
   for (; i < n; i += stride) {
     float4 p = __ldg(pm + i);
     bad |= !finite4(p);
+    mm = fmaxf(mm, fabsf(p.w));
     lo0 = fminf(lo0, p.x); hi0 = fmaxf(hi0, p.x);
     lo1 = fminf(lo1, p.y); hi1 = fmaxf(hi1, p.y);
     lo2 = fminf(lo2, p.z); hi2 = fmaxf(hi2, p.z);
@@ -78,25 +81,28 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
     hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
     hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
     hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
   }
   bad = __any_sync(0xffffffffu, bad);
-  __shared__ float s[6][kBboxThreads / 32];
+  __shared__ float s[7][kBboxThreads / 32];
   __shared__ int s_bad[kBboxThreads / 32];
   __shared__ bool s_last;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     s[0][w] = lo0; s[1][w] = lo1; s[2][w] = lo2;
     s[3][w] = hi0; s[4][w] = hi1; s[5][w] = hi2;
+    s[6][w] = mm;
     s_bad[w] = bad;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float4 a = make_float4(s[0][0], s[1][0], s[2][0], 0.f);
-    float4 b = make_float4(s[3][0], s[4][0], s[5][0], 0.f);
+    float4 b = make_float4(s[3][0], s[4][0], s[5][0], s[6][0]);
     int anybad = s_bad[0];
     for (int k = 1; k < kBboxThreads / 32; ++k) {
       a.x = fminf(a.x, s[0][k]); a.y = fminf(a.y, s[1][k]); a.z = fminf(a.z, s[2][k]);
       b.x = fmaxf(b.x, s[3][k]); b.y = fmaxf(b.y, s[4][k]); b.z = fmaxf(b.z, s[5][k]);
+      b.w = fmaxf(b.w, s[6][k]);
       anybad |= s_bad[k];
     }
     a.w = anybad ? 1.f : 0.f;
@@ -112,11 +118,13 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
   __threadfence();
   lo0 = lo1 = lo2 = INFINITY;
   hi0 = hi1 = hi2 = -INFINITY;
+  mm = 0.f;
   bad = false;
   for (int k = threadIdx.x; k < (int)gridDim.x; k += blockDim.x) {
     float4 a = __ldcg(partials + 2 * k), b = __ldcg(partials + 2 * k + 1);
     lo0 = fminf(lo0, a.x); lo1 = fminf(lo1, a.y); lo2 = fminf(lo2, a.z);
     hi0 = fmaxf(hi0, b.x); hi1 = fmaxf(hi1, b.y); hi2 = fmaxf(hi2, b.z);
+    mm = fmaxf(mm, b.w);
     bad |= (a.w != 0.f);
   }
 #pragma unroll
@@ -127,23 +135,27 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
     hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
     hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
     hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+    mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
   }
   bad = __any_sync(0xffffffffu, bad);
   __syncthreads();
   if (lane == 0) {
     s[0][w] = lo0; s[1][w] = lo1; s[2][w] = lo2;
     s[3][w] = hi0; s[4][w] = hi1; s[5][w] = hi2;
+    s[6][w] = mm;
     s_bad[w] = bad;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     float l[3] = {s[0][0], s[1][0], s[2][0]}, h[3] = {s[3][0], s[4][0], s[5][0]};
     int anybad = s_bad[0];
+    float mmax = s[6][0];
     for (int k = 1; k < kBboxThreads / 32; ++k) {
       for (int a = 0; a < 3; ++a) {
         l[a] = fminf(l[a], s[a][k]);
         h[a] = fmaxf(h[a], s[3 + a][k]);
       }
+      mmax = fmaxf(mmax, s[6][k]);
       anybad |= s_bad[k];
     }
     // Cube side: the largest extent (fp32 subtraction); 1 if all coincide.
@@ -152,6 +164,18 @@ bbox_kernel(const float4 *__restrict__ pm, long long n, float4 *partials,
     if (L == 0.f) L = 1.f;
     ctrl->keep.cube[which] = make_float4(l[0], l[1], l[2], L);
     ctrl->keep.scale[which] = __fdiv_rn((float)(1u << bits), L);
+    // Fixed-point moment scales (powers of two): with |m| < 2^(e_m + 1),
+    // (coordinate - lo) < 2^(e_L + 1) and n <= 2^c, a sum over all particles
+    // of m 2^k_m or of m (coordinate - lo) 2^k_x stays below 2^62.
+    int km = 0, kx = 0;
+    if (mmax > 0.f && isfinite(mmax)) {
+      const int c = n > 1 ? 64 - __clzll((unsigned long long)(n - 1)) : 0;
+      const int em = ilogbf(mmax), eL = ilogbf(L);
+      km = 61 - c - em;
+      kx = 60 - c - em - eL;
+    }
+    ctrl->keep.qexp[which][0] = km;
+    ctrl->keep.qexp[which][1] = kx;
     if (anybad) set_err(ctrl, kErrNonFinite);
     if (bump_epoch) ctrl->keep.epoch += 1u;
     ctrl->step.bbox_done[which] = 0;

@@ -96,17 +96,41 @@ def test_tree_bit_exact_and_com(name, leaf_cap):
     par = nodes[1:, 5]
     idx = np.arange(1, nodes.shape[0])
     assert np.all(nodes[par, 3] <= idx) and np.all(idx < nodes[par, 3] + nodes[par, 4])
-    # centre of mass: fp32 sums against fp64.  A leaf adds its c particles in
-    # sequence and each internal node adds <= 8 children, over <= 22 levels,
-    # so the rounding bound is u * (c_max + 8 * 22) relative to the summed
-    # magnitudes (u = 2^-24); twice that is the tolerance.
+    _assert_com_close(com, o)
+
+
+def _assert_com_close(com, o):
+    """Centre of mass against the fp64 oracle.  The GPU sums each cell's
+    mass and mass moments m (x - lo) exactly (64-bit fixed point, prefix
+    differences), from d = x - lo rounded once in fp32 (error <= u L, u =
+    2^-24, L the cube side); the two sums are each rounded once to fp32, their
+    quotient once (<= 3u of com - lo <= L), and adding lo once more (<= u
+    |com|).  So |com - exact| <= u (5 L + |lo|) and the mass is within u
+    (relative), fixed-point quantisation being ~1e-10 smaller at these mass
+    ratios; the tolerances are 6u and 2u."""
     u = 2.0 ** -24
-    leaf = nodes[:, 3] < 0
-    cmax = int(nodes[leaf, 2].max())
-    tol = 2 * u * (cmax + 8 * 22)
     scale = float(o.cube[3]) + float(np.abs(o.cube[:3]).max())
-    np.testing.assert_allclose(com[:, :3], o.com[:, :3], rtol=0, atol=tol * scale)
-    np.testing.assert_allclose(com[:, 3], o.com[:, 3], rtol=tol)
+    np.testing.assert_allclose(com[:, :3], o.com[:, :3], rtol=0, atol=6 * u * scale)
+    np.testing.assert_allclose(com[:, 3], o.com[:, 3], rtol=2 * u)
+
+
+@pytest.mark.parametrize("leaf_cap", [1, 16])
+def test_com_spread_masses_and_massless_cells(leaf_cap):
+    """Masses log-uniform over six decades, and a tight cluster of massless
+    particles far from the rest (its cells take their geometric centres)."""
+    rng = W.rng(61)
+    src = W.plummer(20000, seed=61)
+    src[:, 3] = (10.0 ** rng.uniform(-6, 0, size=20000)).astype(np.float32)
+    src[-300:, :3] = (1.5 + 1e-3 * rng.random((300, 3))).astype(np.float32)
+    src[-300:, 3] = 0.0
+    bh, _, rc = H.gpu_bh(src, leaf_cap=leaf_cap)
+    assert rc == 0
+    keys, perm, nodes, com, cube = H.export_state(bh, src.shape[0])
+    o = O.OracleBH(src, leaf_cap=leaf_cap)
+    H.assert_tree_equal(nodes, o.tree)
+    assert (o.com[:, 3] == 0).sum() > 0          # some cells hold no mass
+    _assert_com_close(com, o)
+    bh.close()
 
 
 @pytest.mark.parametrize("name", ["uniform4096", "plummer_2e15", "galaxy_2e16", "ragged_12345"])
