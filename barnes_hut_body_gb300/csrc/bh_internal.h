@@ -28,6 +28,19 @@ inline int per_device(std::atomic<int> (&memo)[kMaxDevices], F make) {
   return v;
 }
 
+// Launch a kernel and return the status of that launch alone (not the
+// thread's last error, which may belong to an earlier, unrelated call).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // Number of SMs of the current device (at least 1).
 inline int sm_count() {
   static std::atomic<int> memo[kMaxDevices];

@@ -497,6 +497,68 @@ __device__ __forceinline__ unsigned compact3(unsigned long long key, int axis) {
   return q;
 }
 
+// Centre of mass and mass of node c from its two moment prefixes (every
+// operation explicitly rounded, so any thread computing a node gets the
+// same bits); a massless node takes its cell's centre.
+__device__ __forceinline__ float4 node_com(long long c, const unsigned long long *skeys,
+                                           long long n, int bits, const int4 *topo,
+                                           const unsigned char *level, const long long *pq,
+                                           const long long *tile_pre, float4 cube, int km,
+                                           int kx, int4 &t, int &lvl) {
+  t = topo[c];
+  lvl = level[c];
+  const long long first = t.x < 0 ? 0 : (t.x > n ? n : t.x);
+  const long long end = t.y < first ? first : (t.y > n ? n : t.y);
+  // prefixes at first and end: the node's tile-relative values plus the
+  // prefix before the tile each position falls in
+  const longlong2 *q = reinterpret_cast<const longlong2 *>(pq + 8 * c);
+  const longlong2 *tf = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (first / kBuildTile));
+  const longlong2 *te = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (end / kBuildTile));
+  longlong2 f0 = q[0], f1 = q[1], e0 = q[2], e1 = q[3];
+  const longlong2 tf0 = tf[0], tf1 = tf[1], te0 = te[0], te1 = te[1];
+  f0.x += tf0.x; f0.y += tf0.y; f1.x += tf1.x; f1.y += tf1.y;
+  e0.x += te0.x; e0.y += te0.y; e1.x += te1.x; e1.y += te1.y;
+  const long long dm = e0.x - f0.x;
+  if (dm != 0) {
+    // com - lo = (sum m d 2^kx) / (sum m 2^km) * 2^(km - kx)
+    const float fm = __ll2float_rn(dm);
+    const int sc = km - kx;
+    return make_float4(
+        __fadd_rn(cube.x, ldexpf(__fdiv_rn(__ll2float_rn(e0.y - f0.y), fm), sc)),
+        __fadd_rn(cube.y, ldexpf(__fdiv_rn(__ll2float_rn(e1.x - f1.x), fm), sc)),
+        __fadd_rn(cube.z, ldexpf(__fdiv_rn(__ll2float_rn(e1.y - f1.y), fm), sc)),
+        ldexpf(fm, -km));
+  }
+  const float w = ldexpf(cube.w, -lvl);                 // massless: cell centre
+  const unsigned long long key = skeys[first < n ? first : 0];
+  const int sh = bits - lvl;
+  float ctr[3];
+  const float lo[3] = {cube.x, cube.y, cube.z};
+  for (int a = 0; a < 3; ++a) {
+    const unsigned cell = compact3(key, a) >> sh;
+    ctr[a] = __fadd_rn(lo[a], __fmul_rn(__fadd_rn((float)cell, 0.5f), w));
+  }
+  return make_float4(ctr[0], ctr[1], ctr[2], 0.f);
+}
+
+// Per internal node, the factor F that lets the walk accept all children at
+// once: with r the largest distance from the node's centre of mass to a
+// child's, every child's centre lies at least d - r from a target box that
+// is d from the node's (distance to a set is 1-Lipschitz), and a child's
+// opening test w_c^2/theta^2 < d_c^2 (w_c = w/2) then holds whenever
+// d^2 > (w^2/theta^2) (1/2 + theta r / w)^2.  F = that factor times 1 + 1e-4
+// (so fp32 rounding of either test cannot part them), rounded up to a
+// multiple of 2^-16 and stored as F 2^16 in flags bits 16..31 when F < 1;
+// 0 = never (an opened node has d^2 <= w^2/theta^2, so F >= 1 cannot hold).
+__device__ __forceinline__ unsigned children_factor(float r2max, float w, float theta) {
+  const float rho = __fdiv_ru(__fsqrt_ru(r2max), w);
+  const float f = __fmaf_ru(theta, rho, 0.5f);
+  const float F = __fmul_ru(__fmul_ru(f, f), 1.0001f);
+  if (!(F < 1.f)) return 0u;
+  const float q = ceilf(__fmul_ru(F, 65536.f));
+  return q >= 65535.f ? 0u : (unsigned)q;
+}
+
 __global__ void __launch_bounds__(256)
 com_kernel(const unsigned long long *__restrict__ skeys, long long n, int bits,
            float theta, const int4 *__restrict__ topo,
@@ -512,54 +574,57 @@ com_kernel(const unsigned long long *__restrict__ skeys, long long n, int bits,
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
        c < total; c += stride) {
-    const int4 t = topo[c];
-    const int lvl = level[c];
-    const bool leaf = t.z < 0;
-    long long first = t.x < 0 ? 0 : (t.x > n ? n : t.x);
-    long long end = t.y < first ? first : (t.y > n ? n : t.y);
-    // prefixes at first and end: the node's tile-relative values plus the
-    // prefix before the tile each position falls in
-    const longlong2 *q = reinterpret_cast<const longlong2 *>(pq + 8 * c);
-    const longlong2 *tf = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (first / kBuildTile));
-    const longlong2 *te = reinterpret_cast<const longlong2 *>(tile_pre + 4 * (end / kBuildTile));
-    longlong2 f0 = q[0], f1 = q[1], e0 = q[2], e1 = q[3];
-    const longlong2 tf0 = tf[0], tf1 = tf[1], te0 = te[0], te1 = te[1];
-    f0.x += tf0.x; f0.y += tf0.y; f1.x += tf1.x; f1.y += tf1.y;
-    e0.x += te0.x; e0.y += te0.y; e1.x += te1.x; e1.y += te1.y;
-    const long long dm = e0.x - f0.x;
+    int4 t;
+    int lvl;
     NodeRec r;
+    r.com = node_com(c, skeys, n, bits, topo, level, pq, tile_pre, cube, km, kx, t, lvl);
+    const bool leaf = t.z < 0;
+    const long long first = t.x < 0 ? 0 : (t.x > n ? n : t.x);
+    const long long end = t.y < first ? first : (t.y > n ? n : t.y);
     const float w = ldexpf(cube.w, -lvl);            // full cell edge
-    if (dm != 0) {
-      // com - lo = (sum m d 2^kx) / (sum m 2^km) * 2^(km - kx)
-      const float fm = __ll2float_rn(dm);
-      const int sc = km - kx;
-      r.com = make_float4(
-          __fadd_rn(cube.x, ldexpf(__fdiv_rn(__ll2float_rn(e0.y - f0.y), fm), sc)),
-          __fadd_rn(cube.y, ldexpf(__fdiv_rn(__ll2float_rn(e1.x - f1.x), fm), sc)),
-          __fadd_rn(cube.z, ldexpf(__fdiv_rn(__ll2float_rn(e1.y - f1.y), fm), sc)),
-          ldexpf(fm, -km));
-    } else {                                          // massless: cell centre
-      const unsigned long long key = skeys[first < n ? first : 0];
-      const int sh = bits - lvl;
-      float ctr[3];
-      const float lo[3] = {cube.x, cube.y, cube.z};
-      for (int a = 0; a < 3; ++a) {
-        unsigned cell = compact3(key, a) >> sh;
-        ctr[a] = lo[a] + ((float)cell + 0.5f) * w;
-      }
-      r.com = make_float4(ctr[0], ctr[1], ctr[2], 0.f);
-    }
     r.ropen2 = __fdiv_rn(__fmul_rn(w, w), th2);
     if (leaf) {
       r.link = (int)first;
       r.count = (int)(end - first);
     } else {
       const int nch = t.w - t.z;
+      const bool ok = nch >= 1 && nch <= 8 && t.w <= total && t.z > c;
       r.link = t.z;
-      r.count = (nch >= 1 && nch <= 8 && t.w <= total) ? nch : 0;
+      r.count = ok ? nch : 0;
     }
     r.flags = (leaf ? 1 : 0) | (lvl << 8);
     rec[c] = r;
+  }
+}
+
+// Per internal node, from the finished records: the largest distance from
+// its centre of mass to a child's, turned into the children factor (flags
+// bits 16..31).  Only the node's own thread writes its flags; other threads
+// read only centres of mass, which no thread writes here.
+__global__ void __launch_bounds__(256)
+children_factor_kernel(NodeRec *rec, int bits, float theta,
+                       const DevCtrl *__restrict__ ctrl, long long cap_nodes) {
+  const float L = ctrl->keep.cube[0].w;
+  long long total = 0;
+  for (int l = 0; l <= bits; ++l) total += ctrl->step.level_total[l];
+  if (total > cap_nodes || !(theta > 0.f)) return;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+       c < total; c += stride) {
+    const int4 q = *reinterpret_cast<const int4 *>(&rec[c].ropen2);  // (ro2, link, count, flags)
+    const int flags = q.w, link = q.y, count = q.z;
+    if ((flags & 1) || count < 1 || count > 8 || link <= c || link + count > total) continue;
+    const float4 cp = __ldg(reinterpret_cast<const float4 *>(rec + c));
+    float r2max = 0.f;
+    for (int k = link; k < link + count; ++k) {
+      const float4 ck = __ldg(reinterpret_cast<const float4 *>(rec + k));
+      const float dx = __fsub_rn(ck.x, cp.x), dy = __fsub_rn(ck.y, cp.y),
+                  dz = __fsub_rn(ck.z, cp.z);
+      r2max = fmaxf(r2max, __fadd_ru(__fadd_ru(__fmul_ru(dx, dx), __fmul_ru(dy, dy)),
+                                     __fmul_ru(dz, dz)));
+    }
+    const float w = ldexpf(L, -((flags >> 8) & 255));
+    rec[c].flags = flags | (int)(children_factor(r2max, w, theta) << 16);
   }
 }
 
@@ -578,13 +643,27 @@ cudaError_t launch_build(const unsigned long long *skeys, const float4 *spm,
                                 (int)kWriteDynSmem) == cudaSuccess ? 1 : -1;
   });
   if (opted < 0) return cudaErrorInvalidValue;
-  build_count_kernel<<<(unsigned)ntiles, kBuildThreads, 0, s>>>(
+  {
+    const cudaError_t le = launch_k(build_count_kernel, dim3((unsigned)ntiles), dim3(kBuildThreads), 0, s,
       skeys, n, leaf_cap, bits, b.tile_counts, (int)ntiles);
-  build_scan_kernel<<<bits + 1, kScanThreads, 0, s>>>(b.tile_counts, (int)ntiles, ctrl);
-  build_write_kernel<<<(unsigned)ntiles, kBuildThreads, kWriteDynSmem, s>>>(
+    if (le != cudaSuccess) return le;
+  }
+  {
+    const cudaError_t le = launch_k(build_scan_kernel, dim3(bits + 1), dim3(kScanThreads), 0, s,
+                                    b.tile_counts, (int)ntiles, ctrl);
+    if (le != cudaSuccess) return le;
+  }
+  {
+    const cudaError_t le = launch_k(build_write_kernel, dim3((unsigned)ntiles), dim3(kBuildThreads), kWriteDynSmem, s,
       skeys, spm, n, leaf_cap, bits, b.tile_counts, b.tile_q, (int)ntiles, ctrl,
       b.topo, b.parent, b.level, b.arrive, b.pq, b.cap_nodes);
-  tile_prefix_kernel<<<4, kScanThreads, 0, s>>>(b.tile_q, (int)ntiles);
+    if (le != cudaSuccess) return le;
+  }
+  {
+    const cudaError_t le = launch_k(tile_prefix_kernel, dim3(4), dim3(kScanThreads), 0, s,
+                                    b.tile_q, (int)ntiles);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -593,8 +672,17 @@ cudaError_t launch_com(const float4 *spm, const unsigned long long *skeys,
                        DevCtrl *ctrl, cudaStream_t s) {
   (void)spm;
   int blocks = sm_count() * 8;
-  com_kernel<<<blocks, 256, 0, s>>>(skeys, n, bits, theta, b.topo, b.level, b.pq,
+  {
+    const cudaError_t le = launch_k(com_kernel, dim3(blocks), dim3(256), 0, s,
+                                    skeys, n, bits, theta, b.topo, b.level, b.pq,
                                     b.tile_q, b.rec, ctrl, b.cap_nodes);
+    if (le != cudaSuccess) return le;
+  }
+  {
+    const cudaError_t le = launch_k(children_factor_kernel, dim3(blocks), dim3(256), 0, s,
+                                    b.rec, bits, theta, ctrl, b.cap_nodes);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

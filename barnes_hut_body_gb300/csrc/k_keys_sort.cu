@@ -644,8 +644,12 @@ cudaError_t launch_bbox(const float4 *pm, long long n, float4 *partials,
   long long want = (n + kBboxThreads * 4 - 1) / (kBboxThreads * 4);
   int blocks = (int)(want < max_blocks ? want : max_blocks);
   if (blocks < 1) blocks = 1;
-  bbox_kernel<<<blocks, kBboxThreads, 0, s>>>(pm, n, partials, ctrl, which,
+  {
+    const cudaError_t le = launch_k(bbox_kernel, dim3(blocks), dim3(kBboxThreads), 0, s,
+                                    pm, n, partials, ctrl, which,
                                                bits, bump_epoch ? 1 : 0);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -661,13 +665,17 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
   long long cap = (long long)sm_count() * (n >= (1LL << 21) ? 8 : 4);
   int blocks = (int)(want < cap ? want : cap);
   if (blocks < 1) blocks = 1;
-  keys_kernel<<<blocks, kKeysThreads, 0, s>>>(pm, n, keys, ctrl, which, bits);
+  {
+    const cudaError_t le = launch_k(keys_kernel, dim3(blocks), dim3(kKeysThreads), 0, s,
+                                    pm, n, keys, ctrl, which, bits);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
 template <int ITEMS>
-void sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
-                 unsigned spin_limit, int *final_buf, cudaStream_t s) {
+cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
+                        unsigned spin_limit, int *final_buf, cudaStream_t s) {
   static std::atomic<int> attr[kMaxDevices];
   const size_t smem = sizeof(SortSmem<ITEMS>);
   per_device(attr, [smem] {
@@ -688,16 +696,23 @@ void sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
     unsigned *ctr = &ctrl->step.tile_ctr[which][p];
     unsigned tag = (unsigned)(which * 8 + p);
     if (p == 0)
-      sort_pass_kernel<true, ITEMS><<<(unsigned)grid, kSortThreads, smem, s>>>(
+      {
+        const cudaError_t le = launch_k(sort_pass_kernel<true, ITEMS>, dim3((unsigned)grid), dim3(kSortThreads), smem, s,
           b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
+        if (le != cudaSuccess) return le;
+      }
     else
-      sort_pass_kernel<false, ITEMS><<<(unsigned)grid, kSortThreads, smem, s>>>(
+      {
+        const cudaError_t le = launch_k(sort_pass_kernel<false, ITEMS>, dim3((unsigned)grid), dim3(kSortThreads), smem, s,
           b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
           hist, ctr, b.status, tag, ctrl, spin_limit);
+        if (le != cudaSuccess) return le;
+      }
     cur ^= 1;
   }
   *final_buf = cur;
+  return cudaSuccess;
 }
 
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
@@ -711,8 +726,11 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
                            (int)sizeof(SmallSortSmem));
       return 1;
     });
-    sort_small_kernel<<<1, kSmallSortThreads, sizeof(SmallSortSmem), s>>>(
+    {
+      const cudaError_t le = launch_k(sort_small_kernel, dim3(1), dim3(kSmallSortThreads), sizeof(SmallSortSmem), s,
         b.keys[0], n, passes, b.keys[1], b.idx[1]);
+      if (le != cudaSuccess) return le;
+    }
     *final_buf = 1;
     return cudaGetLastError();
   }
@@ -720,10 +738,8 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
   if (tiles_small > b.cap_tiles) return cudaErrorInvalidValue;
   // 4096-key tiles once 3072-key tiles outnumber the resident blocks
   if (tiles_small > 2LL * sm_count())
-    sort_passes<kSortItemsLarge>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
-  else
-    sort_passes<kSortItemsSmall>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
-  return cudaGetLastError();
+    return sort_passes<kSortItemsLarge>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
+  return sort_passes<kSortItemsSmall>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
 }
 
 cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
@@ -732,7 +748,11 @@ cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
   long long cap = (long long)sm_count() * 16;
   int blocks = (int)(want < cap ? want : cap);
   if (blocks < 1) blocks = 1;
-  gather_kernel<<<blocks, 256, 0, s>>>(in, perm, n, out);
+  {
+    const cudaError_t le = launch_k(gather_kernel, dim3(blocks), dim3(256), 0, s,
+                                    in, perm, n, out);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

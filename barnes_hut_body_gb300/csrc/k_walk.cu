@@ -86,6 +86,19 @@ __device__ __forceinline__ void list_put(WarpSmem &S, int j, float4 v) {
   w[6 + h] = v.w;
 }
 
+// Whether all children of an opened node pass the box test: the node's box
+// distance d2 against its opening radius times the factor the build stored
+// in flags bits 16..31 (0 = never).
+__device__ __forceinline__ bool children_accepted(float d2, float ro2, int flags) {
+  const unsigned f = (unsigned)flags >> 16;
+  return f != 0u && ro2 * __uint2float_rn(f) * (1.f / 65536.f) < d2;
+}
+
+// A list entry (x, y, z, m): particle j, or the centre of mass of node j.
+__device__ __forceinline__ float4 entry_source(const WalkArgs &a, bool node, long long j) {
+  return node ? __ldg(reinterpret_cast<const float4 *>(a.rec + j)) : __ldg(a.spm + j);
+}
+
 // Targets are held duplicated in both fp32 lanes (P = (p, p)); a pair of
 // entries then gives two interactions per packed instruction.  Per pair and
 // target: 3 sub, 3 fma, 2 rsqrt, 3 mul, 3 fma, 1 sub (13 packed + 2 MUFU).
@@ -339,11 +352,13 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       int count = __float_as_int(q.z);
       const int flags = __float_as_int(q.w);
       bool acc = false;
+      float d2 = 0.f;
       if (has) {
         float dx = fmaxf(fmaxf(bl0 - c4.x, c4.x - bh0), 0.f);
         float dy = fmaxf(fmaxf(bl1 - c4.y, c4.y - bh1), 0.f);
         float dz = fmaxf(fmaxf(bl2 - c4.z, c4.z - bh2), 0.f);
-        acc = ro2 < fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+        d2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+        acc = ro2 < d2;
       }
       if (kVote) {
         // Probe pre-test: if one of the probe targets (real targets of the
@@ -388,6 +403,9 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
                             (long long)link + count <= nnodes;
       const bool open_leaf = has && !acc && leaf && link >= 0 && link <= a.n;
       if (open_leaf && count > a.n - link) count = (int)(a.n - link);
+      // an opened node whose children all pass the box test: its children
+      // go to the list without being tested
+      const bool kids = open_int && children_accepted(d2, ro2, flags);
 
       // ---- accepted nodes -> interaction list ---------------------------
       const unsigned am = __ballot_sync(0xffffffffu, has && acc);
@@ -395,10 +413,11 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       nl += __popc(am);
 
       // ---- opened internal nodes -> stack -------------------------------
-      const unsigned om = __ballot_sync(0xffffffffu, open_int);
+      const bool push = open_int && !kids;
+      const unsigned om = __ballot_sync(0xffffffffu, push);
       const int npush = __popc(om);
       if (sp + npush <= kStackCap) {
-        if (open_int)
+        if (push)
           S.stack[sp + __popc(om & lt)] =
               ((unsigned)link << 3) | (unsigned)(count - 1);
         sp += npush;
@@ -407,10 +426,11 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
       }
       __syncwarp();
 
-      // ---- opened leaves -> their particles -----------------------------
-      const unsigned lm = __ballot_sync(0xffffffffu, open_leaf);
+      // ---- opened leaves -> their particles; accepted children ----------
+      const bool expand = open_leaf || kids;
+      const unsigned lm = __ballot_sync(0xffffffffu, expand);
       if (lm) {
-        const int pc = open_leaf ? (count > 0 ? count : 0) : 0;
+        const int pc = expand ? (count > 0 ? count : 0) : 0;
         const int ppre = warp_incl_scan(pc, lane);
         const int ptotal = __shfl_sync(0xffffffffu, ppre, 31);
         const int pexcl = ppre - pc;
@@ -449,8 +469,9 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
           const int owner = lo > 31 ? 31 : lo;
           const int of = __shfl_sync(0xffffffffu, link, owner);
           const int oe = __shfl_sync(0xffffffffu, pexcl, owner);
+          const bool okid = __shfl_sync(0xffffffffu, (int)kids, owner) != 0;
           float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (qi < ptotal) pv = __ldg(a.spm + of + (qi - oe));
+          if (qi < ptotal) pv = entry_source(a, okid, of + (qi - oe));
           if (nl >= kFlushAt) flush_front(S, accum, nl, nvalid, executed);
           if (qi < ptotal) list_put(S, nl + lane, pv);
           nl += (ptotal - base < 32) ? (ptotal - base) : 32;
@@ -695,11 +716,13 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
       int count = __float_as_int(q.z);
       const int flags = __float_as_int(q.w);
       bool acc = false;
+      float d2 = 0.f;
       if (has) {
         float dx = fmaxf(fmaxf(bl0 - c4.x, c4.x - bh0), 0.f);
         float dy = fmaxf(fmaxf(bl1 - c4.y, c4.y - bh1), 0.f);
         float dz = fmaxf(fmaxf(bl2 - c4.z, c4.z - bh2), 0.f);
-        acc = ro2 < fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+        d2 = fmaf(dx, dx, fmaf(dy, dy, dz * dz));
+        acc = ro2 < d2;
       }
       if (kVote) {
         bool und = has && !acc;
@@ -737,16 +760,20 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
                             (unsigned)link > node && (long long)link + count <= nnodes;
       const bool open_leaf = has && !acc && leaf && link >= 0 && link <= a.n;
       if (open_leaf && count > a.n - link) count = (int)(a.n - link);
+      // an opened node whose children all pass the box test (children_factor
+      // of the build): its children go to the list without being tested
+      const bool kids = open_int && children_accepted(d2, ro2, flags);
 
       // accepted nodes -> list
       const unsigned am = __ballot_sync(0xffffffffu, has && acc);
       append(has && acc, __popc(am & lt), __popc(am), c4);
 
       // opened internal nodes -> stack
-      const unsigned om = __ballot_sync(0xffffffffu, open_int);
+      const bool push = open_int && !kids;
+      const unsigned om = __ballot_sync(0xffffffffu, push);
       const int npush = __popc(om);
       if (sp + npush <= kStackCap) {
-        if (open_int)
+        if (push)
           S.stack[sp + __popc(om & lt)] = ((unsigned)link << 3) | (unsigned)(count - 1);
         sp += npush;
       } else if (npush) {
@@ -754,10 +781,11 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
       }
       __syncwarp();
 
-      // opened leaves -> their particles
-      const unsigned lm = __ballot_sync(0xffffffffu, open_leaf);
+      // opened leaves -> their particles; accepted children -> their records
+      const bool expand = open_leaf || kids;
+      const unsigned lm = __ballot_sync(0xffffffffu, expand);
       if (lm) {
-        const int pc = open_leaf ? (count > 0 ? count : 0) : 0;
+        const int pc = expand ? (count > 0 ? count : 0) : 0;
         const int ppre = warp_incl_scan(pc, lane);
         const int ptotal = __shfl_sync(0xffffffffu, ppre, 31);
         const int pexcl = ppre - pc;
@@ -792,8 +820,9 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
           const int owner = lo > 31 ? 31 : lo;
           const int of = __shfl_sync(0xffffffffu, link, owner);
           const int oe = __shfl_sync(0xffffffffu, pexcl, owner);
+          const bool okid = __shfl_sync(0xffffffffu, (int)kids, owner) != 0;
           float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (qi < ptotal) pv = __ldg(a.spm + of + (qi - oe));
+          if (qi < ptotal) pv = entry_source(a, okid, of + (qi - oe));
           const int nput = (ptotal - base < 32) ? (ptotal - base) : 32;
           append(qi < ptotal, lane, nput, pv);
           __syncwarp();
@@ -992,7 +1021,11 @@ cudaError_t launch_ws(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
   const long long need = (ngroups + kWsPairs - 1) / kWsPairs;
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;
-  walk_ws_kernel<T, kVote, kEps0, kSelf><<<(unsigned)blocks, kWsThreads, 0, s>>>(a, ctrl);
+  {
+    const cudaError_t le = launch_k(walk_ws_kernel<T, kVote, kEps0, kSelf>, dim3((unsigned)blocks), dim3(kWsThreads), 0, s,
+                                    a, ctrl);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -1017,7 +1050,11 @@ cudaError_t launch_one(const WalkArgs &a, DevCtrl *ctrl, cudaStream_t s) {
   long long need = (ngroups + kWalkWarps - 1) / kWalkWarps;
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;
-  walk_kernel<T, kVote, kEps0, kSelf><<<(unsigned)blocks, kWalkThreads, 0, s>>>(a, ctrl);
+  {
+    const cudaError_t le = launch_k(walk_kernel<T, kVote, kEps0, kSelf>, dim3((unsigned)blocks), dim3(kWalkThreads), 0, s,
+                                    a, ctrl);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -1121,12 +1158,19 @@ cudaError_t launch_group_order(const unsigned int *cost, long long ngroups,
   if (ngroups <= 0) return cudaSuccess;
   long long blocks = (ngroups + kOrderThreads - 1) / kOrderThreads;
   if (blocks > 4LL * num_sms) blocks = 4LL * num_sms;
-  group_class_count_kernel<<<(unsigned)blocks, kOrderThreads, 0, s>>>(cost, ngroups,
+  {
+    const cudaError_t le = launch_k(group_class_count_kernel, dim3((unsigned)blocks), dim3(kOrderThreads), 0, s,
+                                    cost, ngroups,
                                                                         ctrl->step.sched_cnt);
+    if (le != cudaSuccess) return le;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  group_place_kernel<<<(unsigned)blocks, kOrderThreads, 0, s>>>(
+  {
+    const cudaError_t le = launch_k(group_place_kernel, dim3((unsigned)blocks), dim3(kOrderThreads), 0, s,
       cost, ngroups, ctrl->step.sched_cnt, ctrl->step.sched_fill, order);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 

@@ -60,8 +60,8 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
     and m separate targets unless m is None) bbox, keys and the order (8
     radix passes, or one kernel up to ONE_BLOCK_SORT_MAX keys, + gather; or
     the tree order's histogram, top levels, insert, node count, count and
-    place kernels); then build count/scan/write/tile prefix, centre of mass,
-    the group schedule (on a repeated call with more walk groups than 16 per
+    place kernels); then build count/scan/write/tile prefix, centre of mass
+    and children factors, the group schedule (on a repeated call with more walk groups than 16 per
     SM) and walk."""
     def per_set(rows: int) -> int:
         if order != "radix":
@@ -70,7 +70,7 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
     targets = n if m is None else m
     groups = -(-targets // walk_group(targets))
     sched = 2 if scheduled and groups > 16 * sms else 0     # class counts, placement
-    return per_set(n) + (0 if m is None else per_set(m)) + 6 + sched
+    return per_set(n) + (0 if m is None else per_set(m)) + 7 + sched
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 29.91e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
@@ -852,9 +852,9 @@ def run_stochastic(args, rank, local_rank, world):
                               "evaluations_per_query": ex_d / m, "pot_abs_error": err_d},
             "error_sample": "4096 targets (PCG64 seed 7) against the direct-sum kernel",
             # per step: bbox, keys, 8 radix passes, gather, 4 build passes,
-            # centre of mass, the targets' bbox/keys/8 passes/gather, strata,
+            # centre of mass and children factors, the targets' bbox/keys/8 passes/gather, strata,
             # stochastic walk
-            "gpu_launches": (18 if tgt is None else 29) * args.steps}), flush=True)
+            "gpu_launches": (19 if tgt is None else 30) * args.steps}), flush=True)
     return 0
 
 
