@@ -73,7 +73,7 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
     return per_set(n) + (0 if m is None else per_set(m)) + 7 + sched
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = 29.91e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
+WALK_TRAFFIC_BYTES = 114.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
