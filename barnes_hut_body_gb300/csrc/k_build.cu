@@ -274,35 +274,54 @@ build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
 constexpr int kScanThreads = 1024;
 
 // Exclusive scan, in place, of vals[0], vals[stride], ..., vals[(count-1)
-// stride] by one block; returns the total.
+// stride] by one block; returns the total.  Each thread takes kScanPer
+// consecutive values per chunk (one chunk covers 4096 values: 4M keys).
+constexpr int kScanPer = 4;
+
 template <typename T>
 __device__ long long block_scan_column(T *vals, long long stride, int count) {
   __shared__ long long s_warp[kScanThreads / 32];
-  __shared__ long long s_carry;
+  __shared__ long long s_carry, s_chunk;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (threadIdx.x == 0) s_carry = 0;
   __syncthreads();
-  for (int base = 0; base < count; base += kScanThreads) {
-    const int t = base + threadIdx.x;
-    const long long v = t < count ? (long long)vals[stride * t] : 0;
-    long long x = v;
+  for (int base = 0; base < count; base += kScanThreads * kScanPer) {
+    const int t0 = base + threadIdx.x * kScanPer;
+    long long v[kScanPer];
+    long long run = 0;                       // this thread's values
+#pragma unroll
+    for (int u = 0; u < kScanPer; ++u) {
+      v[u] = t0 + u < count ? (long long)vals[stride * (t0 + u)] : 0;
+      run += v[u];
+    }
+    long long x = run;                       // inclusive over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      long long y = __shfl_up_sync(0xffffffffu, x, o);
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     if (lane == 31) s_warp[w] = x;
     __syncthreads();
-    long long off = 0, all = 0;
-    for (int k = 0; k < kScanThreads / 32; ++k) {
-      const long long q = s_warp[k];
-      if (k < w) off += q;
-      all += q;
+    if (w == 0) {                            // the warps' totals, exclusive
+      const long long tw = s_warp[lane];
+      long long xw = tw;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, xw, o);
+        if (lane >= o) xw += y;
+      }
+      s_warp[lane] = xw - tw;
+      if (lane == 31) s_chunk = xw;
     }
-    const long long carry = s_carry;
-    if (t < count) vals[stride * t] = (T)(carry + off + x - v);
     __syncthreads();
-    if (threadIdx.x == 0) s_carry = carry + all;
+    long long acc = s_carry + s_warp[w] + (x - run);
+#pragma unroll
+    for (int u = 0; u < kScanPer; ++u) {
+      if (t0 + u < count) vals[stride * (t0 + u)] = (T)acc;
+      acc += v[u];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += s_chunk;
     __syncthreads();
   }
   return s_carry;
@@ -559,7 +578,7 @@ __device__ __forceinline__ unsigned children_factor(float r2max, float w, float 
   return q >= 65535.f ? 0u : (unsigned)q;
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 5)
 com_kernel(const unsigned long long *__restrict__ skeys, long long n, int bits,
            float theta, const int4 *__restrict__ topo,
            const unsigned char *__restrict__ level, const long long *__restrict__ pq,
@@ -615,11 +634,15 @@ children_factor_kernel(NodeRec *rec, int bits, float theta,
     const int flags = q.w, link = q.y, count = q.z;
     if ((flags & 1) || count < 1 || count > 8 || link <= c || link + count > total) continue;
     const float4 cp = __ldg(reinterpret_cast<const float4 *>(rec + c));
+    float4 ck[8];                            // all children's loads in flight
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ck[k] = __ldg(reinterpret_cast<const float4 *>(rec + link + (k < count ? k : 0)));
     float r2max = 0.f;
-    for (int k = link; k < link + count; ++k) {
-      const float4 ck = __ldg(reinterpret_cast<const float4 *>(rec + k));
-      const float dx = __fsub_rn(ck.x, cp.x), dy = __fsub_rn(ck.y, cp.y),
-                  dz = __fsub_rn(ck.z, cp.z);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float dx = __fsub_rn(ck[k].x, cp.x), dy = __fsub_rn(ck[k].y, cp.y),
+                  dz = __fsub_rn(ck[k].z, cp.z);
       r2max = fmaxf(r2max, __fadd_ru(__fadd_ru(__fmul_ru(dx, dx), __fmul_ru(dy, dy)),
                                      __fmul_ru(dz, dz)));
     }
