@@ -598,7 +598,7 @@ __device__ __forceinline__ void ws_producer(const WalkArgs &a, DevCtrl *ctrl, Ws
   const unsigned lt = (1u << lane) - 1u;
   constexpr int GS = 32 * T;
   const long long gend = a.g_end;       // groups [g_begin, g_end) of this call
-  unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0, done = 0;
+  unsigned st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0, done = 0;
   unsigned eph = 0;              // parity of the next wait on each empty barrier
   int b = 0, nl = 0;
   bool alive = mb_wait(&S.empty[0], 0);
