@@ -281,6 +281,14 @@ int bh_set_debug(bh_ctx *c, int key, long long value);
  * synchronises the device once; all other calls are fully asynchronous and
  * can be captured in a CUDA graph.  Non-finite positions or masses set
  * BH_EINVAL in the device status word (results are then unspecified).
+ *
+ * Self mode with eps > 0: when a particle's own leaf is opened, its own
+ * pair adds exactly m_i/eps to -phi_i and nothing to a_i, and the walk takes
+ * it back out after the sum; the potential then carries an extra rounding
+ * error of at most about k * 2^-24 * (m_i / eps) (k = terms evaluated for
+ * the particle, typically 10^3), negligible unless eps is far below
+ * m_i / |phi_i| (at the benchmark settings m_i/eps is 1e-4 of |phi_i| or
+ * less).  bh_direct gives the own pair no term at all.
  */
 int bh_compute(bh_ctx *c, const float *pos_mass, size_t n,
                const float *targets, size_t m, float *acc_pot, void *stream);
