@@ -36,7 +36,7 @@ BH_DBG_SPIN_LIMIT = 1
 BH_LF_ACC_VALID = 1
 (BH_EXPORT_CUBE, BH_EXPORT_KEYS, BH_EXPORT_PERM, BH_EXPORT_NODE_COUNT,
  BH_EXPORT_NODES, BH_EXPORT_COM, BH_EXPORT_TARGET_PERM, BH_EXPORT_WALK_STATS,
- BH_EXPORT_GROUP_COST, BH_EXPORT_GROUP_ORDER) = range(1, 11)
+ BH_EXPORT_GROUP_COST, BH_EXPORT_GROUP_ORDER, BH_EXPORT_SORT_PATH) = range(1, 12)
 STAGES = ("bbox", "keys", "sort", "reorder", "build", "com", "targets", "traverse")
 
 EXPORTED = ("bh_create", "bh_destroy", "bh_set_params", "bh_set_option",
@@ -315,6 +315,8 @@ def bh_debug_export(ctx, what: int, count: int = 0) -> np.ndarray:
         out = np.zeros((count, 4), np.float32)
     elif what == BH_EXPORT_WALK_STATS:
         out = np.zeros(4, np.uint64)
+    elif what == BH_EXPORT_SORT_PATH:
+        out = np.zeros(2, np.uint32)
     else:
         raise ValueError("unknown export key")
     _check(ctx, lib().bh_debug_export(ctx, int(what), C.c_void_p(out.ctypes.data), out.nbytes))

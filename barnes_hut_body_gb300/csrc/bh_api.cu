@@ -325,9 +325,11 @@ cudaError_t enqueue_order(bh_ctx *c, const float4 *pm, long long n, int bits, So
       e = launch_order_place(pm, sb.keys[0], n, bits, c->order_bufs, sb.keys[1],
                              sb.idx[1], sorted, c->ctrl, c->num_sms, s);
   } else {
-    e = launch_sort(sb, n, bits, c->ctrl, which, c->spin_limit, fb, s);
+    const unsigned int *gather_skip = nullptr;
+    e = launch_sort(sb, n, bits, c->ctrl, which, c->spin_limit, pm, sorted, fb,
+                    &gather_skip, s);
     if (rec >= 0) record(c, rec, s);
-    if (e == cudaSuccess) e = launch_gather(pm, sb.idx[*fb], n, sorted, s);
+    if (e == cudaSuccess) e = launch_gather(pm, sb.idx[*fb], n, sorted, gather_skip, s);
   }
   return e;
 }
@@ -961,6 +963,10 @@ int bh_debug_export(bh_ctx *c, int what, void *dst, size_t bytes) {
     case BH_EXPORT_WALK_STATS:
       if (!need(32)) return fail(c, BH_EINVAL, "buffer too small");
       memcpy(dst, st.walk_stats, 32);
+      break;
+    case BH_EXPORT_SORT_PATH:
+      if (!need(8)) return fail(c, BH_EINVAL, "buffer too small");
+      memcpy(dst, st.bucket_sort, 8);
       break;
     case BH_EXPORT_NODE_COUNT:
       if (!need(8)) return fail(c, BH_EINVAL, "buffer too small");

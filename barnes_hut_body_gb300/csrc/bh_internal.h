@@ -122,7 +122,11 @@ constexpr unsigned kErrOverflow = BH_ETREE_OVERFLOW;
 // every bh_compute (so no kernel relies on state left by an earlier call).
 struct StepCtrl {
   unsigned int hist[2][kMaxPasses][256];   // digit histograms: sources, targets
-  unsigned int tile_ctr[2][kMaxPasses];    // radix tile tickets per pass
+  unsigned int hist_top[2][256];           // 63-bit keys: histogram of bits 55..62
+  unsigned int tile_ctr[2][kMaxPasses + 1];  // radix tile tickets per pass (+ the
+                                           // top-digit pass)
+  unsigned int bucket_sort[2];             // 1: every top-digit bucket fits one
+                                           // block, the bucket sort ordered the keys
   unsigned int bbox_done[2];               // blocks finished in the bbox pass
   unsigned int work_ctr;                   // traversal group tickets
   int strata;                              // stochastic walk: strata found
@@ -185,11 +189,18 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
                         DevCtrl *ctrl, int which, int bits, cudaStream_t s);
 // Sorts keys[0] (with implicit iota values); the result lands in
 // keys[final]/idx[final], final returned through *final_buf.
+// Sort the keys in sb.keys[0] (ties by index) into sb.keys[*final_buf] and
+// the permutation into sb.idx[*final_buf].  63-bit keys may take the bucket
+// path, which also writes the gathered rows (pm in key order) to `sorted`;
+// the gather must then be told to skip through *gather_skip (a device flag,
+// or NULL when the gather always runs).
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
-                        int which, unsigned spin_limit, int *final_buf,
+                        int which, unsigned spin_limit, const float4 *pm, float4 *sorted,
+                        int *final_buf, const unsigned int **gather_skip,
                         cudaStream_t s);
 cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
-                          long long n, float4 *out, cudaStream_t s);
+                          long long n, float4 *out, const unsigned int *skip_if,
+                          cudaStream_t s);
 
 // Tree-topology order (k_order.cu): an insertion tree over the Morton digits
 // then the index digits of every particle; its depth-first slot order is the

@@ -33,6 +33,15 @@ __device__ __forceinline__ void set_err(DevCtrl *c, unsigned code) {
   atomicCAS(&c->keep.err, 0u, code);
 }
 
+// The top digit of a 63-bit key (bit 63 is always 0): bits 55..62, the
+// octree's first two levels and two bits of the third.
+constexpr int kTopShift = 55;
+// The bucket sort: one block of kBucketThreads threads holds a bucket of up
+// to kBucketCap keys (kBucketItems per thread) in shared memory.
+constexpr int kBucketThreads = 512;
+constexpr int kBucketItems = 9;
+constexpr int kBucketCap = kBucketThreads * kBucketItems;   // 4608 keys
+
 __device__ __forceinline__ bool finite4(float4 p) {
   return isfinite(p.x) && isfinite(p.y) && isfinite(p.z) && isfinite(p.w);
 }
@@ -210,14 +219,15 @@ __global__ void __launch_bounds__(kKeysThreads)
 keys_kernel(const float4 *__restrict__ pm, long long n,
             unsigned long long *__restrict__ keys, DevCtrl *ctrl, int which,
             int bits) {
-  __shared__ unsigned int h[kMaxPasses][256];
-  for (int k = threadIdx.x; k < kMaxPasses * 256; k += blockDim.x)
+  __shared__ unsigned int h[kMaxPasses + 1][256];   // + bits 55..62 of 63-bit keys
+  for (int k = threadIdx.x; k < (kMaxPasses + 1) * 256; k += blockDim.x)
     (&h[0][0])[k] = 0u;
   __syncthreads();
   const float4 cube = ctrl->keep.cube[which];
   const float s = ctrl->keep.scale[which];
   const float top = (float)((1u << bits) - 1u);
   const int passes = (3 * bits + 7) / 8;
+  const int hists = passes + (bits == kMaxBits ? 1 : 0);
   const int lane = threadIdx.x & 31;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long base = (long long)blockIdx.x * blockDim.x; base < n;
@@ -236,8 +246,8 @@ keys_kernel(const float4 *__restrict__ pm, long long n,
     // Spatially ordered input makes whole warps share the high digits: add
     // those with one atomic; otherwise every lane adds its own.
     const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-    for (int ps = 0; ps < passes; ++ps) {
-      const unsigned d = (unsigned)(key >> (8 * ps)) & 255u;
+    for (int ps = 0; ps < hists; ++ps) {
+      const unsigned d = (unsigned)(key >> (ps < passes ? 8 * ps : kTopShift)) & 255u;
       const unsigned d0 = __shfl_sync(0xffffffffu, d, 0);
       if (__all_sync(0xffffffffu, !valid || d == d0)) {
         if (lane == 0) atomicAdd(&h[ps][d0], (unsigned)__popc(vmask));
@@ -252,6 +262,11 @@ keys_kernel(const float4 *__restrict__ pm, long long n,
     unsigned v = (&h[0][0])[k];
     if (v) atomicAdd(gh + k, v);
   }
+  if (hists > passes)
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) {
+      unsigned v = h[passes][k];
+      if (v) atomicAdd(&ctrl->step.hist_top[which][k], v);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -372,13 +387,29 @@ sort_pass_kernel(const unsigned long long *__restrict__ kin,
                  int shift, const unsigned int *__restrict__ hist,
                  unsigned int *tile_ctr, unsigned long long *status,
                  unsigned int tag_base, DevCtrl *ctrl,
-                 unsigned int spin_limit) {
+                 unsigned int spin_limit, const unsigned int *skip_if,
+                 unsigned int *decide) {
   extern __shared__ __align__(128) unsigned char sort_smem_raw[];
   constexpr int kTile = kSortThreads * ITEMS;
   SortSmem<ITEMS> &S = *reinterpret_cast<SortSmem<ITEMS> *>(sort_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // a regular digit pass has nothing to do once the bucket sort ran
+  if (skip_if && *skip_if) return;
+  if (decide) {
+    // the top-digit pass runs only if every bucket fits one block of the
+    // bucket sort; every block finds the same answer, block 0 publishes it
+    unsigned mx = __reduce_max_sync(0xffffffffu, hist[tid]);
+    if (lane == 0) S.warp[w] = mx;
+    __syncthreads();
+    mx = 0;
+    for (int k = 0; k < kSortThreads / 32; ++k) mx = S.warp[k] > mx ? S.warp[k] : mx;
+    __syncthreads();
+    const bool fits = mx <= (unsigned)kBucketCap;
+    if (blockIdx.x == 0 && tid == 0) *decide = fits ? 1u : 0u;
+    if (!fits) return;
+  }
   const unsigned long long tag =
-      (unsigned long long)(tag_base + ctrl->keep.epoch * 16u) << 32;
+      (unsigned long long)(tag_base + ctrl->keep.epoch * 32u) << 32;
 
   auto issue = [&](int b, long long t) {
     // keys (and indices) of tile t into stage b; sizes rounded up to 16
@@ -625,9 +656,161 @@ sort_small_kernel(const unsigned long long *__restrict__ kin, long long n, int p
   }
 }
 
+// ---------------------------------------------------------------------------
+// Bucket sort: after one pass on the top digit (bits 55..62), the keys sit
+// in 256 buckets, each already in index order.  When every bucket holds at
+// most kBucketCap keys, one block per bucket sorts its keys on bits 0..54 in
+// shared memory (7 digit passes, the same warp-ballot ranking, so the same
+// stable order) and writes the final keys, indices and gathered rows -- one
+// kernel in place of seven global passes and the gather.
+// ---------------------------------------------------------------------------
+constexpr int kBucketWarps = kBucketThreads / 32;
+constexpr int kBucketPasses = 7;
+
+struct BucketSmem {
+  alignas(16) unsigned long long k[kBucketCap];
+  alignas(16) unsigned int v[kBucketCap];
+  unsigned int whist[kBucketWarps * kSmallRow];
+  unsigned int dig[256];
+  unsigned int warp[kBucketWarps];
+  unsigned int off;
+};
+
+__global__ void __launch_bounds__(kBucketThreads, 2)
+bucket_sort_kernel(const unsigned long long *__restrict__ kin,
+                   const unsigned int *__restrict__ vin, long long n,
+                   const unsigned int *__restrict__ hist_top,
+                   const unsigned int *__restrict__ go,
+                   unsigned long long *__restrict__ kout, unsigned int *__restrict__ vout,
+                   const float4 *__restrict__ pm, float4 *__restrict__ sorted) {
+  if (!*go) return;
+  extern __shared__ __align__(128) unsigned char bucket_raw[];
+  BucketSmem &S = *reinterpret_cast<BucketSmem *>(bucket_raw);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int b = blockIdx.x;
+  // this bucket's start: the counts of the buckets before it
+  {
+    unsigned c = tid < b ? hist_top[tid] : 0u;   // b < 256 <= kBucketThreads
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) S.warp[w] = c;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned o = 0;
+      for (int k = 0; k < kBucketWarps; ++k) o += S.warp[k];
+      S.off = o;
+    }
+    __syncthreads();
+  }
+  const long long off = S.off;
+  const int cnt = (int)hist_top[b];
+  if (cnt == 0 || off + cnt > n || cnt > kBucketCap) return;
+  // padding keys (all ones) sort after the real ones; every load is issued
+  // before the first store so the bucket arrives in one memory latency
+  {
+    unsigned long long kk[kBucketItems];
+    unsigned int vv[kBucketItems];
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      const int j = i * kBucketThreads + tid;
+      kk[i] = j < cnt ? kin[off + j] : ~0ull;
+      vv[i] = j < cnt ? vin[off + j] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      S.k[i * kBucketThreads + tid] = kk[i];
+      S.v[i * kBucketThreads + tid] = vv[i];
+    }
+  }
+  // warp-items wholly past the last key (rounded up to 32) are padding in
+  // every pass: padding keys are the largest and start last, so a stable
+  // pass leaves them where they are, and they are neither ranked nor moved
+  const int live = (cnt + 31) & ~31;
+  const int wbase = w * (kBucketItems * 32);
+  for (int p = 0; p < kBucketPasses; ++p) {
+    const int shift = 8 * p;
+    for (int k = tid; k < kBucketWarps * kSmallRow; k += kBucketThreads) S.whist[k] = 0u;
+    __syncthreads();                       // counts zeroed, keys in place
+    unsigned long long key[kBucketItems];
+    unsigned int val[kBucketItems], rnk[kBucketItems];
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      const int j = wbase + i * 32 + lane;
+      key[i] = S.k[j];
+      val[i] = S.v[j];
+    }
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i)
+      if (wbase + i * 32 < live)
+        rnk[i] = warp_rank((unsigned)(key[i] >> shift) & 255u, &S.whist[w * kSmallRow], lt);
+    __syncthreads();                       // every warp holds its keys: the buffer is free
+    // per digit (thread d < 256): the warps' offsets and the digit's total
+    if (tid < 256) {
+      unsigned run = 0;
+#pragma unroll
+      for (int k = 0; k < kBucketWarps; ++k) {
+        const unsigned c = S.whist[k * kSmallRow + tid];
+        S.whist[k * kSmallRow + tid] = run;
+        run += c;
+      }
+      S.dig[tid] = run;
+    }
+    __syncthreads();
+    // start of each digit: exclusive scan of the 256 totals (8 per lane)
+    if (w == 0) {
+      unsigned t[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { t[q] = S.dig[lane * 8 + q]; sum += t[q]; }
+      unsigned x = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      unsigned run = x - sum;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) { S.dig[lane * 8 + q] = run; run += t[q]; }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      if (wbase + i * 32 < live) {
+        const unsigned d = (unsigned)(key[i] >> shift) & 255u;
+        const unsigned pos = S.dig[d] + S.whist[w * kSmallRow + d] + rnk[i];
+        S.k[pos] = key[i];
+        S.v[pos] = val[i];
+      }
+    }
+    __syncthreads();                       // scattered; the counts may be cleared
+  }
+  // write out: all row loads in flight at once
+  {
+    unsigned int vv[kBucketItems];
+    float4 rr[kBucketItems];
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      const int j = i * kBucketThreads + tid;
+      vv[i] = S.v[j];
+      rr[i] = (j < cnt && vv[i] < (unsigned long long)n) ? __ldg(pm + vv[i])
+                                                         : make_float4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kBucketItems; ++i) {
+      const int j = i * kBucketThreads + tid;
+      if (j < cnt) {
+        kout[off + j] = S.k[j];
+        vout[off + j] = vv[i];
+        sorted[off + j] = rr[i];
+      }
+    }
+  }
+}
+
 __global__ void gather_kernel(const float4 *__restrict__ in,
                               const unsigned int *__restrict__ perm,
-                              long long n, float4 *__restrict__ out) {
+                              long long n, float4 *__restrict__ out,
+                              const unsigned int *__restrict__ skip_if) {
+  if (skip_if && *skip_if) return;         // the bucket sort wrote the rows
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n;
        r += stride) {
@@ -673,9 +856,9 @@ cudaError_t launch_keys(const float4 *pm, long long n, unsigned long long *keys,
   return cudaGetLastError();
 }
 
+// the digit-pass kernels' shared-memory opt-in, once per device
 template <int ITEMS>
-cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
-                        unsigned spin_limit, int *final_buf, cudaStream_t s) {
+void pass_attributes() {
   static std::atomic<int> attr[kMaxDevices];
   const size_t smem = sizeof(SortSmem<ITEMS>);
   per_device(attr, [smem] {
@@ -685,6 +868,14 @@ cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return 1;
   });
+}
+
+template <int ITEMS>
+cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int which,
+                        unsigned spin_limit, int *final_buf, const unsigned int *skip_if,
+                        cudaStream_t s) {
+  pass_attributes<ITEMS>();
+  const size_t smem = sizeof(SortSmem<ITEMS>);
   constexpr long long kTile = (long long)kSortThreads * ITEMS;
   const long long tiles = (n + kTile - 1) / kTile;
   long long grid = (long long)sm_count() * 2;
@@ -694,19 +885,19 @@ cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int
   for (int p = 0; p < passes; ++p) {
     const unsigned *hist = &ctrl->step.hist[which][p][0];
     unsigned *ctr = &ctrl->step.tile_ctr[which][p];
-    unsigned tag = (unsigned)(which * 8 + p);
+    unsigned tag = (unsigned)(which * 16 + p);
     if (p == 0)
       {
         const cudaError_t le = launch_k(sort_pass_kernel<true, ITEMS>, dim3((unsigned)grid), dim3(kSortThreads), smem, s,
           b.keys[cur], nullptr, b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
-          hist, ctr, b.status, tag, ctrl, spin_limit);
+          hist, ctr, b.status, tag, ctrl, spin_limit, skip_if, nullptr);
         if (le != cudaSuccess) return le;
       }
     else
       {
         const cudaError_t le = launch_k(sort_pass_kernel<false, ITEMS>, dim3((unsigned)grid), dim3(kSortThreads), smem, s,
           b.keys[cur], b.idx[cur], b.keys[cur ^ 1], b.idx[cur ^ 1], n, tiles, 8 * p,
-          hist, ctr, b.status, tag, ctrl, spin_limit);
+          hist, ctr, b.status, tag, ctrl, spin_limit, skip_if, nullptr);
         if (le != cudaSuccess) return le;
       }
     cur ^= 1;
@@ -715,10 +906,45 @@ cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int
   return cudaSuccess;
 }
 
+// 63-bit keys: the top-digit pass into buffer 1, then the bucket sort back
+// into buffer 0 (with the rows gathered); both do nothing unless every
+// top-digit bucket fits one block, which the top pass decides on the device.
+template <int ITEMS>
+cudaError_t bucket_path(SortBufs &b, long long n, DevCtrl *ctrl, int which,
+                        unsigned spin_limit, const float4 *pm, float4 *sorted,
+                        cudaStream_t s) {
+  static std::atomic<int> attr[kMaxDevices];
+  per_device(attr, [] {
+    cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(BucketSmem));
+    return 1;
+  });
+  pass_attributes<ITEMS>();
+  const size_t smem = sizeof(SortSmem<ITEMS>);
+  constexpr long long kTile = (long long)kSortThreads * ITEMS;
+  const long long tiles = (n + kTile - 1) / kTile;
+  long long grid = (long long)sm_count() * 2;
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
+  unsigned *flag = &ctrl->step.bucket_sort[which];
+  const unsigned *top = &ctrl->step.hist_top[which][0];
+  cudaError_t e = launch_k(sort_pass_kernel<true, ITEMS>, dim3((unsigned)grid),
+                           dim3(kSortThreads), smem, s, b.keys[0], nullptr, b.keys[1],
+                           b.idx[1], n, tiles, kTopShift, top,
+                           &ctrl->step.tile_ctr[which][kMaxPasses], b.status,
+                           (unsigned)(which * 16 + kMaxPasses), ctrl, spin_limit, nullptr,
+                           flag);
+  if (e != cudaSuccess) return e;
+  return launch_k(bucket_sort_kernel, dim3(256), dim3(kBucketThreads), sizeof(BucketSmem), s,
+                  b.keys[1], b.idx[1], n, top, flag, b.keys[0], b.idx[0], pm, sorted);
+}
+
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
-                        int which, unsigned spin_limit, int *final_buf,
+                        int which, unsigned spin_limit, const float4 *pm, float4 *sorted,
+                        int *final_buf, const unsigned int **gather_skip,
                         cudaStream_t s) {
   const int passes = (3 * bits + 7) / 8;
+  *gather_skip = nullptr;
   if (n <= kSmallSortN) {
     static std::atomic<int> attr[kMaxDevices];
     per_device(attr, [] {
@@ -737,20 +963,32 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
   const long long tiles_small = (n + kSortTile - 1) / kSortTile;
   if (tiles_small > b.cap_tiles) return cudaErrorInvalidValue;
   // 4096-key tiles once 3072-key tiles outnumber the resident blocks
-  if (tiles_small > 2LL * sm_count())
-    return sort_passes<kSortItemsLarge>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
-  return sort_passes<kSortItemsSmall>(b, n, passes, ctrl, which, spin_limit, final_buf, s);
+  const bool large = tiles_small > 2LL * sm_count();
+  const unsigned *skip = nullptr;
+  if (bits == kMaxBits) {
+    // the bucket path first; the digit passes and the gather then do
+    // nothing if it ran (same final buffer either way)
+    cudaError_t e = large ? bucket_path<kSortItemsLarge>(b, n, ctrl, which, spin_limit, pm, sorted, s)
+                          : bucket_path<kSortItemsSmall>(b, n, ctrl, which, spin_limit, pm, sorted, s);
+    if (e != cudaSuccess) return e;
+    skip = &ctrl->step.bucket_sort[which];
+    *gather_skip = skip;
+  }
+  if (large)
+    return sort_passes<kSortItemsLarge>(b, n, passes, ctrl, which, spin_limit, final_buf, skip, s);
+  return sort_passes<kSortItemsSmall>(b, n, passes, ctrl, which, spin_limit, final_buf, skip, s);
 }
 
 cudaError_t launch_gather(const float4 *in, const unsigned int *perm,
-                          long long n, float4 *out, cudaStream_t s) {
+                          long long n, float4 *out, const unsigned int *skip_if,
+                          cudaStream_t s) {
   long long want = (n + 255) / 256;
   long long cap = (long long)sm_count() * 16;
   int blocks = (int)(want < cap ? want : cap);
   if (blocks < 1) blocks = 1;
   {
     const cudaError_t le = launch_k(gather_kernel, dim3(blocks), dim3(256), 0, s,
-                                    in, perm, n, out);
+                                    in, perm, n, out, skip_if);
     if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();

@@ -56,21 +56,28 @@ ONE_BLOCK_SORT_MAX = 4096
 
 def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
                      scheduled: bool = True) -> int:
-    """Our kernels per step with 63-bit keys: per particle set (n sources,
-    and m separate targets unless m is None) bbox, keys and the order (8
-    radix passes, or one kernel up to ONE_BLOCK_SORT_MAX keys, + gather; or
+    """Our kernels per step (63-bit source keys, 30-bit target keys): per
+    particle set (n sources, and m separate targets unless m is None) bbox,
+    keys and the order (the radix passes, one per 8 key bits, preceded for
+    63-bit keys by the top-digit pass and the bucket sort, or one kernel up to
+    ONE_BLOCK_SORT_MAX keys, + gather; or
     the tree order's histogram, top levels, insert, node count, count and
     place kernels); then build count/scan/write/tile prefix, centre of mass
     and children factors, the group schedule (on a repeated call with more walk groups than 16 per
     SM) and walk."""
-    def per_set(rows: int) -> int:
+    def per_set(rows: int, key_bits: int) -> int:
         if order != "radix":
             return 2 + 6
-        return 2 + (1 if rows <= ONE_BLOCK_SORT_MAX else 8) + 1
+        if rows <= ONE_BLOCK_SORT_MAX:
+            return 2 + 1 + 1
+        passes = (key_bits + 7) // 8
+        # 63-bit keys: the top-digit pass and the bucket sort come first (the
+        # digit passes and the gather then return at once when they ran)
+        return 2 + (2 if key_bits == 63 else 0) + passes + 1
     targets = n if m is None else m
     groups = -(-targets // walk_group(targets))
     sched = 2 if scheduled and groups > 16 * sms else 0     # class counts, placement
-    return per_set(n) + (0 if m is None else per_set(m)) + 7 + sched
+    return per_set(n, 63) + (0 if m is None else per_set(m, 30)) + 7 + sched
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 114.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture

@@ -217,6 +217,13 @@ typedef struct bh_ctx bh_ctx;
 #define BH_EXPORT_GROUP_ORDER 10 /* uint32[groups]: the order the call handed
                                     its groups to the walk; BH_EINVAL if it
                                     used Morton order                        */
+#define BH_EXPORT_SORT_PATH   11 /* uint32[2]: 1 where the keys of the sources
+                                    (then of separate targets) were sorted by
+                                    the bucket path (63-bit keys, every bucket
+                                    of bits 55..62 within 4608 keys: one pass
+                                    on those bits, then each bucket sorted in
+                                    shared memory), 0 where the digit passes
+                                    ran; the permutation is the same        */
 
 /* Stage indices for bh_get_stage_times. */
 #define BH_STAGE_BBOX      0

@@ -1,0 +1,131 @@
+"""The sort's bucket path against the oracle.
+
+With 63-bit keys the sort first sorts on the top digit (key bits 55..62: the
+octree's first two levels and two bits of the third); when every one of those
+256 buckets holds at most 4608 keys, one block per bucket finishes it in
+shared memory and writes the rows in key order, and the digit passes and the
+gather do nothing.  Otherwise the digit passes run as before.  Either way the
+permutation must be the oracle's stable sort (ties by index) bit for bit and
+everything after it the same; BH_EXPORT_SORT_PATH says which path ran.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+BUCKET_CAP = 4608
+
+
+def _with_bucket_of(count, seed=71):
+    """50,000 uniform points plus a tight cluster inside one top-digit
+    bucket, so that this bucket (the largest) holds exactly `count` keys."""
+    base = W.uniform_cube(50000, seed=seed)
+    cube = O.bbox(base)
+    g = W.rng(seed)
+    cluster = np.zeros((count, 4), np.float32)
+    cluster[:, :3] = (0.2 + 1e-4 * g.random((count, 3))).astype(np.float32)
+    cluster[:, 3] = base[0, 3]
+    key = O.keys(cluster[:1], cube, 21)[0]
+    top = int(key >> np.uint64(55))
+    have = int(((O.keys(base, cube, 21) >> np.uint64(55)) == top).sum())
+    src = np.ascontiguousarray(np.concatenate([base, cluster[:count - have]]), np.float32)
+    # the points stay inside the uniform points' box, so the cube is unchanged
+    tops = (O.keys(src, O.bbox(src), 21) >> np.uint64(55)).astype(np.int64)
+    counts = np.bincount(tops, minlength=256)
+    assert counts[top] == count and counts.max() == count
+    return src
+
+
+def _check(src, tgt=None, walk=True, **opts):
+    import barnes_hut_body_gb300 as B
+    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, eps=1e-3, group=64, **opts)
+    assert rc == 0
+    path = B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)
+    n = src.shape[0]
+    keys, perm, nodes, com, cube = H.export_state(bh, n)
+    o = O.OracleBH(src, theta=0.5, eps=1e-3, leaf_cap=16)
+    np.testing.assert_array_equal(perm, o.perm)
+    np.testing.assert_array_equal(keys, o.skeys)
+    H.assert_tree_equal(nodes, o.tree)
+    from tests.test_gpu_parity import _assert_com_close
+    _assert_com_close(com, o)
+    if not walk:
+        return bh, path, got
+    ref, rows, terms, mag = o.bh_group(tgt, group=64, mode=0, with_abs=True)
+    # the cluster's targets sum thousands of near-equal softened terms: fp32
+    # recursive summation is then good only to about (terms) * 2^-24
+    sizes = np.diff(np.append(np.arange(0, rows.size, 64), rows.size))
+    H.assert_walk_close(got[rows], ref, "bucket sort", mag, nterms=np.repeat(terms, sizes))
+    return bh, path, got
+
+
+@pytest.mark.parametrize("count,path", [(BUCKET_CAP, 1), (BUCKET_CAP + 1, 0)])
+def test_bucket_limit(count, path):
+    """Largest bucket at the limit (bucket path) and one key past it (digit
+    passes): identical permutation, tree, centres of mass and forces."""
+    bh, got_path, _ = _check(_with_bucket_of(count))
+    assert int(got_path[0]) == path
+    bh.close()
+
+
+def test_lattice_takes_the_bucket_path():
+    """The 1M lattice (its largest top-digit bucket holds 4225 keys)."""
+    import barnes_hut_body_gb300 as B
+    src = W.lattice(100, permute_seed=1)
+    bh, got, rc = H.gpu_bh(src, theta=0.5, eps=5e-3)
+    assert rc == 0
+    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == 1
+    perm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_PERM, src.shape[0])
+    np.testing.assert_array_equal(perm, O.sort(O.keys(src, O.bbox(src), 21)))
+    bh.close()
+
+
+def test_separate_targets_with_63_bit_keys():
+    """Targets ordered by 63-bit keys take the same path (which = 1)."""
+    import barnes_hut_body_gb300 as B
+    src = W.uniform_cube(30000, seed=72)
+    tgt = W.uniform_cube(120000, seed=73)
+    bh, got, rc = H.gpu_bh(src, tgt, theta=0.5, eps=1e-3, group=64, target_key_bits=21)
+    assert rc == 0
+    assert [int(x) for x in B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)] == [1, 1]
+    tperm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_TARGET_PERM, tgt.shape[0])
+    np.testing.assert_array_equal(tperm, O.sort(O.keys(tgt, O.bbox(tgt), 21)))
+    o = O.OracleBH(src, theta=0.5, eps=1e-3, leaf_cap=16, target_bits=21)
+    ref, rows, _, mag = o.bh_group(tgt, group=64, mode=0, with_abs=True)
+    H.assert_walk_close(got[rows], ref, "targets", mag)
+    bh.close()
+
+
+def test_repeated_calls_replay_the_same_result():
+    """Identical calls (the second and later replay a captured graph) give
+    the same bits on the bucket path."""
+    import torch
+    import barnes_hut_body_gb300 as B
+    src = W.uniform_cube(200000, seed=74)
+    d = H.to_dev(src)
+    bh = B.BarnesHut(theta=0.5, eps=1e-3)
+    outs = [bh.compute(d).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert bh.status() == 0
+    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == 1
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    bh.close()
+
+
+def test_all_points_equal_fall_back():
+    """One bucket holding every key: the digit passes run."""
+    n = 8000
+    src = np.tile(np.array([[0.5, 0.5, 0.5, 1e-3]], np.float32), (n, 1))
+    bh, path, got = _check(src, walk=False)
+    assert int(path[0]) == 0
+    # every pair at distance zero: no force, and the potential is the same
+    # n - 1 softened terms for every particle (fp32 sum of n equal terms)
+    assert np.all(got[:, :3] == 0)
+    ref = O.direct(src, None, 1.0, 1e-3, idx=np.arange(4))
+    np.testing.assert_allclose(got[:, 3], ref[0, 3], rtol=n * 2.0 ** -24)
+    bh.close()
