@@ -162,6 +162,16 @@ struct DevCtrl {
   PersistCtrl keep;
 };
 
+// Nodes of the current tree: the level totals summed over every level (the
+// step's control block starts zeroed and the build writes levels 0..bits
+// only), with all the loads in flight at once.
+__device__ __forceinline__ long long node_total(const DevCtrl *ctrl) {
+  long long t = 0;
+#pragma unroll
+  for (int l = 0; l < kMaxLevels; ++l) t += ctrl->step.level_total[l];
+  return t;
+}
+
 // One traversal record per node, 32 bytes: (com.xyz, mass) and
 // (ropen2 = w^2/theta^2, link, count, flags).  link = first child for an
 // internal node, first particle (sorted index) for a leaf; count = children

@@ -397,15 +397,26 @@ build_write_kernel(const unsigned long long *__restrict__ skeys,
       q_add(run, each[u]);
     }
   }
-  if (threadIdx.x == 0) {
-    long long off = 0;
-    for (int l = 0; l <= bits; ++l) {
-      s_base[l] = off + tile_off[(long long)l * ntiles + tile];
-      off += ctrl->step.level_total[l];
+  if (w == 0) {
+    // level l's first index in this tile: the nodes of the levels above it
+    // (a scan across lanes) plus the tile offset within the level; all the
+    // loads in flight at once
+    const bool in = lane <= bits;
+    const long long tot = in ? ctrl->step.level_total[lane] : 0;
+    const long long toff = in ? tile_off[(long long)lane * ntiles + tile] : 0;
+    long long x = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    s_base[bits + 1] = off;
-    s_ok = off <= cap_nodes;
-    if (!s_ok && tile == 0) set_err(ctrl, kErrOverflow);
+    if (in) s_base[lane] = x - tot + toff;
+    const long long all = __shfl_sync(0xffffffffu, x, 31);
+    if (lane == 0) {
+      s_base[bits + 1] = all;
+      s_ok = all <= cap_nodes;
+      if (!s_ok && tile == 0) set_err(ctrl, kErrOverflow);
+    }
   }
   for (int k = threadIdx.x; k < kBuildIters * kLvWarps * kMaxLevels; k += blockDim.x)
     (&s_cnt[0][0][0])[k] = 0u;
@@ -584,8 +595,7 @@ com_kernel(const unsigned long long *__restrict__ skeys, long long n, int bits,
            const unsigned char *__restrict__ level, const long long *__restrict__ pq,
            const long long *__restrict__ tile_pre, NodeRec *__restrict__ rec,
            const DevCtrl *__restrict__ ctrl, long long cap_nodes) {
-  long long total = 0;
-  for (int l = 0; l <= bits; ++l) total += ctrl->step.level_total[l];
+  const long long total = node_total(ctrl);
   if (total > cap_nodes) return;
   const float4 cube = ctrl->keep.cube[0];
   const int km = ctrl->keep.qexp[0][0], kx = ctrl->keep.qexp[0][1];
@@ -624,8 +634,7 @@ __global__ void __launch_bounds__(256)
 children_factor_kernel(NodeRec *rec, int bits, float theta,
                        const DevCtrl *__restrict__ ctrl, long long cap_nodes) {
   const float L = ctrl->keep.cube[0].w;
-  long long total = 0;
-  for (int l = 0; l <= bits; ++l) total += ctrl->step.level_total[l];
+  const long long total = node_total(ctrl);
   if (total > cap_nodes || !(theta > 0.f)) return;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;

@@ -909,16 +909,11 @@ cudaError_t sort_passes(SortBufs &b, long long n, int passes, DevCtrl *ctrl, int
 // 63-bit keys: the top-digit pass into buffer 1, then the bucket sort back
 // into buffer 0 (with the rows gathered); both do nothing unless every
 // top-digit bucket fits one block, which the top pass decides on the device.
+// (A graph conditional node choosing between this and the digit passes
+// measured slower than letting the idle kernels return at once.)
 template <int ITEMS>
-cudaError_t bucket_path(SortBufs &b, long long n, DevCtrl *ctrl, int which,
-                        unsigned spin_limit, const float4 *pm, float4 *sorted,
-                        cudaStream_t s) {
-  static std::atomic<int> attr[kMaxDevices];
-  per_device(attr, [] {
-    cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(BucketSmem));
-    return 1;
-  });
+cudaError_t top_pass(SortBufs &b, long long n, DevCtrl *ctrl, int which,
+                     unsigned spin_limit, cudaStream_t s) {
   pass_attributes<ITEMS>();
   const size_t smem = sizeof(SortSmem<ITEMS>);
   constexpr long long kTile = (long long)kSortThreads * ITEMS;
@@ -926,17 +921,25 @@ cudaError_t bucket_path(SortBufs &b, long long n, DevCtrl *ctrl, int which,
   long long grid = (long long)sm_count() * 2;
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
-  unsigned *flag = &ctrl->step.bucket_sort[which];
-  const unsigned *top = &ctrl->step.hist_top[which][0];
-  cudaError_t e = launch_k(sort_pass_kernel<true, ITEMS>, dim3((unsigned)grid),
-                           dim3(kSortThreads), smem, s, b.keys[0], nullptr, b.keys[1],
-                           b.idx[1], n, tiles, kTopShift, top,
-                           &ctrl->step.tile_ctr[which][kMaxPasses], b.status,
-                           (unsigned)(which * 16 + kMaxPasses), ctrl, spin_limit, nullptr,
-                           flag);
-  if (e != cudaSuccess) return e;
+  return launch_k(sort_pass_kernel<true, ITEMS>, dim3((unsigned)grid),
+                  dim3(kSortThreads), smem, s, b.keys[0], nullptr, b.keys[1],
+                  b.idx[1], n, tiles, kTopShift, &ctrl->step.hist_top[which][0],
+                  &ctrl->step.tile_ctr[which][kMaxPasses], b.status,
+                  (unsigned)(which * 16 + kMaxPasses), ctrl, spin_limit, nullptr,
+                  &ctrl->step.bucket_sort[which]);
+}
+
+cudaError_t bucket_sort(SortBufs &b, long long n, DevCtrl *ctrl, int which,
+                        const float4 *pm, float4 *sorted, cudaStream_t s) {
+  static std::atomic<int> attr[kMaxDevices];
+  per_device(attr, [] {
+    cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(BucketSmem));
+    return 1;
+  });
   return launch_k(bucket_sort_kernel, dim3(256), dim3(kBucketThreads), sizeof(BucketSmem), s,
-                  b.keys[1], b.idx[1], n, top, flag, b.keys[0], b.idx[0], pm, sorted);
+                  b.keys[1], b.idx[1], n, &ctrl->step.hist_top[which][0],
+                  &ctrl->step.bucket_sort[which], b.keys[0], b.idx[0], pm, sorted);
 }
 
 cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
@@ -968,8 +971,9 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
   if (bits == kMaxBits) {
     // the bucket path first; the digit passes and the gather then do
     // nothing if it ran (same final buffer either way)
-    cudaError_t e = large ? bucket_path<kSortItemsLarge>(b, n, ctrl, which, spin_limit, pm, sorted, s)
-                          : bucket_path<kSortItemsSmall>(b, n, ctrl, which, spin_limit, pm, sorted, s);
+    cudaError_t e = large ? top_pass<kSortItemsLarge>(b, n, ctrl, which, spin_limit, s)
+                          : top_pass<kSortItemsSmall>(b, n, ctrl, which, spin_limit, s);
+    if (e == cudaSuccess) e = bucket_sort(b, n, ctrl, which, pm, sorted, s);
     if (e != cudaSuccess) return e;
     skip = &ctrl->step.bucket_sort[which];
     *gather_skip = skip;

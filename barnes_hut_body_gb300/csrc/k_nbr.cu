@@ -71,8 +71,7 @@ nb_node_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
                long long n, const int4 *__restrict__ topo,
                const int *__restrict__ parent, int *arrive, NbNode *nodes,
                DevCtrl *ctrl, long long cap_nodes) {
-  long long total = 0;
-  for (int l = 0; l < kMaxLevels; ++l) total += ctrl->step.level_total[l];
+  const long long total = node_total(ctrl);
   if (total > cap_nodes) return;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x; c < total;
@@ -164,8 +163,7 @@ nb_walk_kernel(const float4 *__restrict__ spm, const float *__restrict__ sh,
   __shared__ NbWarp smem[kNbWarps];
   NbWarp &W = smem[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  long long nnodes = 0;
-  for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  long long nnodes = node_total(ctrl);
   if (nnodes > nnodes_cap) nnodes = nnodes_cap;
   const long long ngroups = (n + 31) / 32;
   unsigned int *ticket = kFill ? &ctrl->step.fill_ctr : &ctrl->step.work_ctr;

@@ -198,8 +198,7 @@ walk_kernel(WalkArgs a, DevCtrl *ctrl) {
   const long long gend = a.g_end;       // groups [g_begin, g_end) of this call
   unsigned long long executed = 0, ngroup_done = 0;
   unsigned long long st_rounds = 0, st_tested = 0, st_voted = 0, st_chunks = 0;
-  long long nnodes = 0;
-  for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  const long long nnodes = node_total(ctrl);
   if (lane == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&S.bar)) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -948,8 +947,7 @@ walk_ws_kernel(WalkArgs a, DevCtrl *ctrl) {
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
-  long long nnodes = 0;
-  for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  const long long nnodes = node_total(ctrl);
   if (w & 1) ws_consumer<T, kEps0, kSelf>(a, ctrl, S);
   else ws_producer<T, kVote, kEps0, kSelf>(a, ctrl, S, nnodes);
 }
@@ -964,8 +962,7 @@ __global__ void __launch_bounds__(256)
 count_kernel(const NodeRec *__restrict__ rec, const float4 *__restrict__ tpos,
              const unsigned int *__restrict__ tperm, long long m, long long n,
              int self_mode, unsigned int *counts, DevCtrl *ctrl) {
-  long long nnodes = 0;
-  for (int l = 0; l < kMaxLevels; ++l) nnodes += ctrl->step.level_total[l];
+  const long long nnodes = node_total(ctrl);
   unsigned long long local = 0;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < m;

@@ -58,26 +58,33 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
                      scheduled: bool = True) -> int:
     """Our kernels per step (63-bit source keys, 30-bit target keys): per
     particle set (n sources, and m separate targets unless m is None) bbox,
-    keys and the order (the radix passes, one per 8 key bits, preceded for
-    63-bit keys by the top-digit pass and the bucket sort, or one kernel up to
-    ONE_BLOCK_SORT_MAX keys, + gather; or
-    the tree order's histogram, top levels, insert, node count, count and
-    place kernels); then build count/scan/write/tile prefix, centre of mass
-    and children factors, the group schedule (on a repeated call with more walk groups than 16 per
-    SM) and walk."""
+    keys and the order (order_kernels; or the tree order's histogram, top
+    levels, insert, node count, count and place kernels); then build
+    count/scan/write/tile prefix, centre of mass and children factors, the
+    group schedule (on a repeated call with more walk groups than 16 per SM)
+    and walk."""
     def per_set(rows: int, key_bits: int) -> int:
         if order != "radix":
             return 2 + 6
-        if rows <= ONE_BLOCK_SORT_MAX:
-            return 2 + 1 + 1
-        passes = (key_bits + 7) // 8
-        # 63-bit keys: the top-digit pass and the bucket sort come first (the
-        # digit passes and the gather then return at once when they ran)
-        return 2 + (2 if key_bits == 63 else 0) + passes + 1
+        return 2 + order_kernels(rows, key_bits)
     targets = n if m is None else m
     groups = -(-targets // walk_group(targets))
     sched = 2 if scheduled and groups > 16 * sms else 0     # class counts, placement
     return per_set(n, 63) + (0 if m is None else per_set(m, 30)) + 7 + sched
+
+
+def order_kernels(rows: int, key_bits: int) -> int:
+    """Kernels of the radix order (sort + gather) of one particle set: one
+    kernel up to ONE_BLOCK_SORT_MAX keys, else one pass per 8 key bits,
+    preceded for 63-bit keys by the top-digit pass and the bucket sort (the
+    digit passes and the gather then return at once if the bucket sort ran),
+    + gather."""
+    if rows <= ONE_BLOCK_SORT_MAX:
+        return 2
+    passes = (key_bits + 7) // 8
+    return (2 if key_bits == 63 else 0) + passes + 1
+
+
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
 WALK_TRAFFIC_BYTES = 114.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
@@ -874,10 +881,12 @@ def run_stochastic(args, rank, local_rank, world):
             "deterministic": {"theta": theta, "ms_per_step": ms_d,
                               "evaluations_per_query": ex_d / m, "pot_abs_error": err_d},
             "error_sample": "4096 targets (PCG64 seed 7) against the direct-sum kernel",
-            # per step: bbox, keys, 8 radix passes, gather, 4 build passes,
-            # centre of mass and children factors, the targets' bbox/keys/8 passes/gather, strata,
-            # stochastic walk
-            "gpu_launches": (19 if tgt is None else 30) * args.steps}), flush=True)
+            # per step: bbox, keys and the order of the sources (63-bit keys)
+            # and of separate targets (30-bit keys), 4 build passes, centre of
+            # mass and children factors, strata, stochastic walk
+            "gpu_launches": (2 + order_kernels(n, 63) + 6 + 2 +
+                             (0 if tgt is None else 2 + order_kernels(m, 30)))
+                            * args.steps}), flush=True)
     return 0
 
 
@@ -953,9 +962,11 @@ def run_neighbors(args, rank, local_rank, world):
             "pairs": total, "neighbours_per_particle": {"mean": float(c.mean()),
                                                         "max": int(c.max())},
             "pair_tests": tests, "tests_per_pair": tests / max(total, 1),
-            # per call: bbox, keys, 8 radix passes, gather, 4 build passes,
-            # h gather, node boxes, counting walk, 3 scan kernels, list walk
-            "gpu_launches": 22 * args.steps}), flush=True)
+            # per call: bbox, keys, the order (top-digit pass, bucket sort, 8
+            # digit passes, gather), 4 build passes, h gather, node boxes,
+            # counting walk, 3 scan kernels, list walk
+            "gpu_launches": (2 + order_kernels(n, 63) + 4 + 7) * args.steps}),
+          flush=True)
     bh.close()
     return 0
 

@@ -100,20 +100,49 @@ def test_separate_targets_with_63_bit_keys():
     bh.close()
 
 
-def test_repeated_calls_replay_the_same_result():
-    """Identical calls (the second and later replay a captured graph) give
-    the same bits on the bucket path."""
+@pytest.mark.parametrize("case,path", [("uniform", 1), ("over", 0)])
+def test_repeated_calls_replay_the_same_result(case, path):
+    """Identical calls give the same bits whichever path runs (the second
+    call captures a graph of the step, later ones replay it, the device
+    deciding the path on every replay); the permutation after a replay is
+    still the oracle's."""
     import torch
     import barnes_hut_body_gb300 as B
-    src = W.uniform_cube(200000, seed=74)
+    src = W.uniform_cube(200000, seed=74) if case == "uniform" else _with_bucket_of(BUCKET_CAP + 1)
     d = H.to_dev(src)
     bh = B.BarnesHut(theta=0.5, eps=1e-3)
-    outs = [bh.compute(d).clone() for _ in range(3)]
+    buf = torch.empty((src.shape[0], 4), dtype=torch.float32, device=d.device)
+    outs = [bh.compute(d, out=buf).clone() for _ in range(4)]
     torch.cuda.synchronize()
     assert bh.status() == 0
-    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == 1
+    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == path
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+    perm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_PERM, src.shape[0])
+    np.testing.assert_array_equal(perm, O.sort(O.keys(src, O.bbox(src), 21)))
+    bh.close()
+
+
+def test_one_context_switching_between_branches():
+    """One context alternating between inputs that take the two branches
+    (each input repeated, so each is captured and replayed) keeps every
+    result equal to a fresh context's."""
+    import torch
+    import barnes_hut_body_gb300 as B
+    a = H.to_dev(W.uniform_cube(200000, seed=75))
+    b = H.to_dev(_with_bucket_of(BUCKET_CAP + 1, seed=76))
+    ref = {}
+    for name, d in (("a", a), ("b", b)):
+        fresh = B.BarnesHut(theta=0.5, eps=1e-3)
+        ref[name] = fresh.compute(d).clone()
+        fresh.close()
+    bh = B.BarnesHut(theta=0.5, eps=1e-3)
+    bufs = {k: torch.empty_like(v) for k, v in ref.items()}
+    for name, d in (("a", a), ("a", a), ("a", a), ("b", b), ("b", b), ("b", b), ("a", a)):
+        out = bh.compute(d, out=bufs[name])
+        torch.cuda.synchronize()
+        assert bh.status() == 0
+        assert torch.equal(out, ref[name]), name
     bh.close()
 
 
