@@ -968,7 +968,8 @@ cudaError_t launch_sort(SortBufs &b, long long n, int bits, DevCtrl *ctrl,
   // 4096-key tiles once 3072-key tiles outnumber the resident blocks
   const bool large = tiles_small > 2LL * sm_count();
   const unsigned *skip = nullptr;
-  if (bits == kMaxBits) {
+  // with more than 256 * kBucketCap keys some bucket must overflow
+  if (bits == kMaxBits && n <= 256LL * kBucketCap) {
     // the bucket path first; the digit passes and the gather then do
     // nothing if it ran (same final buffer either way)
     cudaError_t e = large ? top_pass<kSortItemsLarge>(b, n, ctrl, which, spin_limit, s)

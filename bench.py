@@ -52,6 +52,9 @@ FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
 # Up to this many keys the radix sort is one kernel (all passes in one block).
 ONE_BLOCK_SORT_MAX = 4096
+# Up to this many 63-bit keys the sort tries the bucket path (256 top-digit
+# buckets of at most 4608 keys each).
+BUCKET_SORT_MAX = 256 * 4608
 
 
 def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
@@ -76,13 +79,15 @@ def kernels_per_step(order: str, n: int, m: int | None, sms: int = 152,
 def order_kernels(rows: int, key_bits: int) -> int:
     """Kernels of the radix order (sort + gather) of one particle set: one
     kernel up to ONE_BLOCK_SORT_MAX keys, else one pass per 8 key bits,
-    preceded for 63-bit keys by the top-digit pass and the bucket sort (the
-    digit passes and the gather then return at once if the bucket sort ran),
+    preceded for 63-bit keys by the top-digit pass and the bucket sort while
+    the 256 top-digit buckets can all fit (rows <= BUCKET_SORT_MAX; the digit
+    passes and the gather then return at once if the bucket sort ran),
     + gather."""
     if rows <= ONE_BLOCK_SORT_MAX:
         return 2
     passes = (key_bits + 7) // 8
-    return (2 if key_bits == 63 else 0) + passes + 1
+    bucket = 2 if key_bits == 63 and rows <= BUCKET_SORT_MAX else 0
+    return bucket + passes + 1
 
 
 # DRAM bytes per walk launch from the committed ncu capture of the same

@@ -219,9 +219,10 @@ typedef struct bh_ctx bh_ctx;
                                     used Morton order                        */
 #define BH_EXPORT_SORT_PATH   11 /* uint32[2]: 1 where the keys of the sources
                                     (then of separate targets) were sorted by
-                                    the bucket path (63-bit keys, every bucket
-                                    of bits 55..62 within 4608 keys: one pass
-                                    on those bits, then each bucket sorted in
+                                    the bucket path (63-bit keys, 4097 to
+                                    256 * 4608 of them, every bucket of bits
+                                    55..62 within 4608 keys: one pass on
+                                    those bits, then each bucket sorted in
                                     shared memory), 0 where the digit passes
                                     ran; the permutation is the same        */
 

@@ -158,3 +158,17 @@ def test_all_points_equal_fall_back():
     ref = O.direct(src, None, 1.0, 1e-3, idx=np.arange(4))
     np.testing.assert_allclose(got[:, 3], ref[0, 3], rtol=n * 2.0 ** -24)
     bh.close()
+
+
+def test_above_the_bucket_capacity_uses_the_digit_passes():
+    """More than 256 * 4608 keys cannot all fit: the digit passes run even
+    for uniform points (whose buckets would each hold ~4700 keys)."""
+    import barnes_hut_body_gb300 as B
+    n = 256 * BUCKET_CAP + 1
+    src = W.uniform_cube(n, seed=77)
+    bh, _, rc = H.gpu_bh(src, theta=0.5, eps=1e-3)
+    assert rc == 0
+    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == 0
+    perm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_PERM, n)
+    np.testing.assert_array_equal(perm, O.sort(O.keys(src, O.bbox(src), 21)))
+    bh.close()
