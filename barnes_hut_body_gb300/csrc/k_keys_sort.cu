@@ -676,6 +676,139 @@ struct BucketSmem {
   unsigned int off;
 };
 
+// One stable 8-bit digit pass over the bucket in shared memory (key bits
+// shift .. shift + 7): warp-ballot ranks, the warps' offsets per digit, the
+// digit starts (left in S.dig), the scatter.  Warp-items wholly past `live`
+// are padding in every pass (padding keys are the largest and start last,
+// so a stable pass leaves them where they are): neither ranked nor moved.
+__device__ __forceinline__ void bucket_pass(BucketSmem &S, int shift, int live, int wbase,
+                                            int tid, int lane, int w, unsigned lt) {
+  for (int k = tid; k < kBucketWarps * kSmallRow; k += kBucketThreads) S.whist[k] = 0u;
+  __syncthreads();                         // counts zeroed, keys in place
+  unsigned long long key[kBucketItems];
+  unsigned int val[kBucketItems], rnk[kBucketItems];
+#pragma unroll
+  for (int i = 0; i < kBucketItems; ++i) {
+    const int j = wbase + i * 32 + lane;
+    key[i] = S.k[j];
+    val[i] = S.v[j];
+  }
+#pragma unroll
+  for (int i = 0; i < kBucketItems; ++i)
+    if (wbase + i * 32 < live)
+      rnk[i] = warp_rank((unsigned)(key[i] >> shift) & 255u, &S.whist[w * kSmallRow], lt);
+  __syncthreads();                         // every warp holds its keys: the buffer is free
+  // per digit (thread d < 256): the warps' offsets and the digit's total
+  if (tid < 256) {
+    unsigned run = 0;
+#pragma unroll
+    for (int k = 0; k < kBucketWarps; ++k) {
+      const unsigned c = S.whist[k * kSmallRow + tid];
+      S.whist[k * kSmallRow + tid] = run;
+      run += c;
+    }
+    S.dig[tid] = run;
+  }
+  __syncthreads();
+  // start of each digit: exclusive scan of the 256 totals (8 per lane)
+  if (w == 0) {
+    unsigned t[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { t[q] = S.dig[lane * 8 + q]; sum += t[q]; }
+    unsigned x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    unsigned run = x - sum;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { S.dig[lane * 8 + q] = run; run += t[q]; }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kBucketItems; ++i) {
+    if (wbase + i * 32 < live) {
+      const unsigned d = (unsigned)(key[i] >> shift) & 255u;
+      const unsigned pos = S.dig[d] + S.whist[w * kSmallRow + d] + rnk[i];
+      S.k[pos] = key[i];
+      S.v[pos] = val[i];
+    }
+  }
+  __syncthreads();                         // scattered; the counts may be cleared
+}
+
+// The bucket's keys share bits 55..62; a first pass on bits 47..54 splits
+// it into 256 sub-buckets whose keys share bits 47..62.  When none holds
+// more than kSubCap keys, each warp sorts whole sub-buckets on the
+// composite (bits 0..46 of the key, position in the sub-bucket) -- unique,
+// and in index order for equal keys, since the passes so far are stable and
+// the bucket started in index order: by counting up to 32 keys (rank =
+// number of smaller composites), by a bitonic network up to 64.  Otherwise
+// the bucket takes the seven digit passes on bits 0..55 (LSD from the
+// current order, which is stable so far, is still the stable sort).
+constexpr int kSubShift = 47;
+constexpr int kSubCap = 64;
+
+__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
+  return a < b ? a : b;
+}
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a < b ? b : a;
+}
+
+// Sort sub-bucket [st, st + sz) (2 <= sz <= kSubCap) of the shared arrays by
+// one warp, in place.
+__device__ __forceinline__ void sort_sub_bucket(BucketSmem &S, int st, int sz, int lane) {
+  constexpr unsigned long long kLow = (1ull << kSubShift) - 1ull;
+  unsigned long long a0 = lane < sz ? ((S.k[st + lane] & kLow) << 6) | (unsigned)lane : ~0ull;
+  unsigned long long a1 = lane + 32 < sz
+                              ? ((S.k[st + lane + 32] & kLow) << 6) | (unsigned)(lane + 32)
+                              : ~0ull;
+  int r0 = lane, r1 = lane + 32;           // ranks of a0, a1 in the sorted sub-bucket
+  if (sz <= 32) {
+    int r = 0;
+    for (int t = 0; t < sz; ++t) r += __shfl_sync(0xffffffffu, a0, t) < a0 ? 1 : 0;
+    r0 = r;
+  } else {
+    // bitonic network over the 64 slots e = lane (a0) and e = lane + 32 (a1)
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        if (j == 32) {
+          const unsigned long long lo = umin64(a0, a1), hi = umax64(a0, a1);
+          a0 = lo;
+          a1 = hi;
+        } else {
+          const unsigned long long v0 = __shfl_xor_sync(0xffffffffu, a0, j);
+          const unsigned long long v1 = __shfl_xor_sync(0xffffffffu, a1, j);
+          const bool lower = (lane & j) == 0;
+          const bool asc0 = (lane & k) == 0, asc1 = ((lane + 32) & k) == 0;
+          a0 = (lower == asc0) ? umin64(a0, v0) : umax64(a0, v0);
+          a1 = (lower == asc1) ? umin64(a1, v1) : umax64(a1, v1);
+        }
+      }
+    }
+  }
+  // counting: this lane's entry goes to rank r0; bitonic: slot e holds rank e
+  unsigned long long k0 = 0, k1 = 0;
+  unsigned v0 = 0, v1 = 0;
+  int i0 = -1, i1 = -1;                    // source positions of what this lane writes
+  if (sz <= 32) {
+    if (lane < sz) i0 = lane;
+  } else {
+    if (lane < sz) i0 = (int)(a0 & 63ull);
+    if (lane + 32 < sz) i1 = (int)(a1 & 63ull);
+  }
+  if (i0 >= 0) { k0 = S.k[st + i0]; v0 = S.v[st + i0]; }
+  if (i1 >= 0) { k1 = S.k[st + i1]; v1 = S.v[st + i1]; }
+  __syncwarp();
+  if (i0 >= 0) { S.k[st + r0] = k0; S.v[st + r0] = v0; }
+  if (i1 >= 0) { S.k[st + r1] = k1; S.v[st + r1] = v1; }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kBucketThreads, 2)
 bucket_sort_kernel(const unsigned long long *__restrict__ kin,
                    const unsigned int *__restrict__ vin, long long n,
@@ -722,66 +855,34 @@ bucket_sort_kernel(const unsigned long long *__restrict__ kin,
       S.v[i * kBucketThreads + tid] = vv[i];
     }
   }
-  // warp-items wholly past the last key (rounded up to 32) are padding in
-  // every pass: padding keys are the largest and start last, so a stable
-  // pass leaves them where they are, and they are neither ranked nor moved
   const int live = (cnt + 31) & ~31;
   const int wbase = w * (kBucketItems * 32);
-  for (int p = 0; p < kBucketPasses; ++p) {
-    const int shift = 8 * p;
-    for (int k = tid; k < kBucketWarps * kSmallRow; k += kBucketThreads) S.whist[k] = 0u;
-    __syncthreads();                       // counts zeroed, keys in place
-    unsigned long long key[kBucketItems];
-    unsigned int val[kBucketItems], rnk[kBucketItems];
+  bucket_pass(S, kSubShift, live, wbase, tid, lane, w, lt);
+  // the largest sub-bucket (real keys only: the padding is digit 255, last)
+  if (tid < 256) {
+    const int st = (int)S.dig[tid];
+    int en = tid < 255 ? (int)S.dig[tid + 1] : live;
+    en = en < cnt ? en : cnt;
+    const unsigned mx = __reduce_max_sync(0xffffffffu, (unsigned)(en > st ? en - st : 0));
+    if (lane == 0) S.warp[w] = mx;
+  }
+  __syncthreads();
+  unsigned mx = 0;
 #pragma unroll
-    for (int i = 0; i < kBucketItems; ++i) {
-      const int j = wbase + i * 32 + lane;
-      key[i] = S.k[j];
-      val[i] = S.v[j];
-    }
-#pragma unroll
-    for (int i = 0; i < kBucketItems; ++i)
-      if (wbase + i * 32 < live)
-        rnk[i] = warp_rank((unsigned)(key[i] >> shift) & 255u, &S.whist[w * kSmallRow], lt);
-    __syncthreads();                       // every warp holds its keys: the buffer is free
-    // per digit (thread d < 256): the warps' offsets and the digit's total
-    if (tid < 256) {
-      unsigned run = 0;
-#pragma unroll
-      for (int k = 0; k < kBucketWarps; ++k) {
-        const unsigned c = S.whist[k * kSmallRow + tid];
-        S.whist[k * kSmallRow + tid] = run;
-        run += c;
-      }
-      S.dig[tid] = run;
+  for (int k = 0; k < 256 / 32; ++k) mx = S.warp[k] > mx ? S.warp[k] : mx;
+  if (mx <= (unsigned)kSubCap) {
+    for (int d = w; d < 256; d += kBucketWarps) {
+      const int st = (int)S.dig[d];
+      int en = d < 255 ? (int)S.dig[d + 1] : live;
+      en = en < cnt ? en : cnt;
+      if (en - st >= 2) sort_sub_bucket(S, st, en - st, lane);
     }
     __syncthreads();
-    // start of each digit: exclusive scan of the 256 totals (8 per lane)
-    if (w == 0) {
-      unsigned t[8], sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { t[q] = S.dig[lane * 8 + q]; sum += t[q]; }
-      unsigned x = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      unsigned run = x - sum;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { S.dig[lane * 8 + q] = run; run += t[q]; }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < kBucketItems; ++i) {
-      if (wbase + i * 32 < live) {
-        const unsigned d = (unsigned)(key[i] >> shift) & 255u;
-        const unsigned pos = S.dig[d] + S.whist[w * kSmallRow + d] + rnk[i];
-        S.k[pos] = key[i];
-        S.v[pos] = val[i];
-      }
-    }
-    __syncthreads();                       // scattered; the counts may be cleared
+  } else {
+    // all seven passes, the last on bits 48..55: LSD from the current order
+    // (stable so far) is the stable sort
+    for (int p = 0; p < kBucketPasses; ++p)
+      bucket_pass(S, 8 * p, live, wbase, tid, lane, w, lt);
   }
   // write out: all row loads in flight at once
   {

@@ -172,3 +172,74 @@ def test_above_the_bucket_capacity_uses_the_digit_passes():
     perm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_PERM, n)
     np.testing.assert_array_equal(perm, O.sort(O.keys(src, O.bbox(src), 21)))
     bh.close()
+
+
+SUB_CAP = 64
+
+
+def _with_sub_buckets(counts, seed=81, spread=1e-5, identical=False):
+    """200,000 uniform points plus, for each c in `counts`, a tight cluster
+    inside its own sub-bucket (keys sharing bits 47..62) topped up so that
+    the sub-bucket holds exactly c keys; identical=True makes each cluster
+    one repeated point (equal keys: ties by index)."""
+    base = W.uniform_cube(200000, seed=seed)
+    cube = O.bbox(base)
+    g = W.rng(seed)
+    parts = [base]
+    sub = (O.keys(base, cube, 21) >> np.uint64(47)).astype(np.int64)
+    have_all = np.bincount(sub, minlength=1 << 16)
+    used = []
+    for c in counts:
+        while True:
+            ctr = (0.05 + 0.9 * g.random(3)).astype(np.float32)
+            probe = np.zeros((1, 4), np.float32)
+            probe[0, :3] = ctr
+            s = int(O.keys(probe, cube, 21)[0] >> np.uint64(47))
+            if s not in used and have_all[s] < c:
+                break
+        used.append(s)
+        extra = c - int(have_all[s])
+        pts = np.zeros((extra, 4), np.float32)
+        pts[:, :3] = ctr if identical else (ctr + spread * g.random((extra, 3))).astype(np.float32)
+        pts[:, 3] = base[0, 3]
+        parts.append(pts)
+    src = np.ascontiguousarray(np.concatenate(parts), np.float32)
+    # the clusters stay inside the uniform points' box and sub-bucket
+    keys = O.keys(src, O.bbox(src), 21)
+    got = np.bincount((keys >> np.uint64(47)).astype(np.int64), minlength=1 << 16)
+    for s, c in zip(used, counts):
+        assert got[s] == c, (got[s], c)
+    return src
+
+
+@pytest.mark.parametrize("counts", [[32], [33], [SUB_CAP], [SUB_CAP + 1],
+                                    [2, 17, 31, 32, 33, 47, 63, SUB_CAP]])
+def test_sub_bucket_sizes(counts):
+    """Sub-buckets sorted by counting (up to 32 keys), by the bitonic
+    network (33 to 64) and, past 64, the whole bucket by digit passes:
+    the permutation and keys are the oracle's either way."""
+    import barnes_hut_body_gb300 as B
+    src = _with_sub_buckets(counts)
+    bh, _, rc = H.gpu_bh(src, theta=0.5, eps=1e-3)
+    assert rc == 0
+    assert int(B.bh_debug_export(bh.ctx, B.BH_EXPORT_SORT_PATH)[0]) == 1
+    n = src.shape[0]
+    keys, perm, nodes, com, cube = H.export_state(bh, n)
+    o = O.OracleBH(src, theta=0.5, eps=1e-3, leaf_cap=16)
+    np.testing.assert_array_equal(perm, o.perm)
+    np.testing.assert_array_equal(keys, o.skeys)
+    H.assert_tree_equal(nodes, o.tree)
+    bh.close()
+
+
+@pytest.mark.parametrize("count", [40, SUB_CAP])
+def test_sub_bucket_of_equal_keys(count):
+    """A sub-bucket of identical points (one key repeated): ties go by index
+    through the bitonic network."""
+    import barnes_hut_body_gb300 as B
+    src = _with_sub_buckets([count], identical=True)
+    bh, _, rc = H.gpu_bh(src, theta=0.5, eps=1e-3)
+    assert rc == 0
+    perm = B.bh_debug_export(bh.ctx, B.BH_EXPORT_PERM, src.shape[0])
+    np.testing.assert_array_equal(perm, O.sort(O.keys(src, O.bbox(src), 21)))
+    bh.close()
