@@ -77,14 +77,40 @@ struct TileGeom {
 // D_j = max of lam over the B + 1 windows [i, i + B] that contain j; the
 // maximum over B + 1 consecutive values comes from a sparse table: the
 // maxima of runs of 2^s values by doubling, then two overlapping runs.
-__device__ void load_geom(TileGeom &g, const unsigned long long *skeys,
-                          long long n, long long tb, int B, int bits) {
+// The tile's keys (with the halos) into shared memory, every load issued
+// before the first store; no barrier.
+constexpr int kKeyLoads = (kBuildTile + 2 * kHalo + 2 + kBuildThreads - 1) / kBuildThreads;
+
+__device__ __forceinline__ void load_keys(TileGeom &g, const unsigned long long *skeys,
+                                          long long n, long long tb, int B) {
   const long long k0 = tb - B - 1;
   const int nk = kBuildTile + 2 * B + 2;
-  for (int x = threadIdx.x; x < nk; x += blockDim.x) {
-    long long i = k0 + x;
-    g.k[x] = (i >= 0 && i < n) ? skeys[i] : 0ull;
+  unsigned long long v[kKeyLoads];
+#pragma unroll
+  for (int u = 0; u < kKeyLoads; ++u) {
+    const int x = threadIdx.x + u * kBuildThreads;
+    const long long i = k0 + x;
+    v[u] = (x < nk && i >= 0 && i < n) ? __ldg(skeys + i) : 0ull;
   }
+#pragma unroll
+  for (int u = 0; u < kKeyLoads; ++u) {
+    const int x = threadIdx.x + u * kBuildThreads;
+    if (x < nk) g.k[x] = v[u];
+  }
+}
+
+// The rest of the geometry once the keys are in place (the first barrier
+// publishes them).
+__device__ void finish_geom(TileGeom &g, long long n, long long tb, int B, int bits);
+
+__device__ void load_geom(TileGeom &g, const unsigned long long *skeys,
+                          long long n, long long tb, int B, int bits) {
+  load_keys(g, skeys, n, tb, B);
+  finish_geom(g, n, tb, B, bits);
+}
+
+__device__ void finish_geom(TileGeom &g, long long n, long long tb, int B, int bits) {
+  const long long k0 = tb - B - 1;
   __syncthreads();
   // lam[y] for i = k0 + y, y in [0, kBuildTile + B + 1)
   const int nl = kBuildTile + B + 1;
@@ -360,6 +386,8 @@ build_write_kernel(const unsigned long long *__restrict__ skeys,
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int tile = blockIdx.x;
   const long long tb = (long long)tile * kBuildTile;
+  // the tile's keys go to shared memory while the particles load
+  load_keys(g, skeys, n, tb, B);
   // the tile's moments: local exclusive prefix at positions
   // tb + kQPer * threadIdx.x + u, and the tile's sums
   {
@@ -420,7 +448,7 @@ build_write_kernel(const unsigned long long *__restrict__ skeys,
   }
   for (int k = threadIdx.x; k < kBuildIters * kLvWarps * kMaxLevels; k += blockDim.x)
     (&s_cnt[0][0][0])[k] = 0u;
-  load_geom(g, skeys, n, tb, B, bits);       // synchronises the block
+  finish_geom(g, n, tb, B, bits);            // synchronises the block
   if (!s_ok) return;
   // phase A: per (iteration, warp, level) counts, over the warp's levels only
   int s[kBuildIters], L[kBuildIters], e[kBuildIters], Lp[kBuildIters];
