@@ -92,7 +92,7 @@ def order_kernels(rows: int, key_bits: int) -> int:
 
 # DRAM bytes per walk launch from the committed ncu capture of the same
 # kernel (profiles/); None until a capture of the current kernel exists.
-WALK_TRAFFIC_BYTES = 114.75e6   # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
+WALK_TRAFFIC_BYTES = 29.84e6    # walk_ws_kernel<2,vote> on lattice1m_shuffled, from that capture
 L2_FLUSH_BYTES = 256 << 20
 
 
