@@ -150,7 +150,7 @@ void free_sources(bh_ctx *c) {
   free_dev(c->spm);
   free_dev(c->build.topo); free_dev(c->build.parent); free_dev(c->build.level);
   free_dev(c->build.arrive); free_dev(c->build.pq); free_dev(c->build.rec);
-  free_dev(c->build.tile_counts); free_dev(c->build.tile_q);
+  free_dev(c->build.tile_counts); free_dev(c->build.tile_q); free_dev(c->build.facts);
   c->cap_n = 0; c->cap_nodes = 0;
 }
 
@@ -227,6 +227,7 @@ int ensure_sources(bh_ctx *c, long long n) {
   ok = ok && alloc_dev(c->build.arrive, nodes);
   ok = ok && alloc_dev(c->build.pq, 8 * nodes);
   ok = ok && alloc_dev(c->build.rec, nodes);
+  ok = ok && alloc_dev(c->build.facts, 2 * cap);
   long long btiles = (cap + 1 + kBuildTile - 1) / kBuildTile;
   ok = ok && alloc_dev(c->build.tile_counts, btiles * kMaxLevels);
   ok = ok && alloc_dev(c->build.tile_q, 4 * btiles);

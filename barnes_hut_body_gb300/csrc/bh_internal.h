@@ -247,6 +247,9 @@ struct BuildBufs {
                          // then at one past its last, each relative to the
                          // start of the build tile holding that position
   NodeRec *rec;
+  signed char *facts;          // [position][2]: the first level at which the
+                               // position starts a cell, and its leaf level
+                               // (the count pass's, for the write pass)
   unsigned int *tile_counts;   // [level][tile]
   long long *tile_q;           // [tile][4]: the tile's moment sums, then the
                                // prefix before the tile

@@ -73,10 +73,6 @@ struct TileGeom {
   signed char D[kBuildTile + 1];             // deepest over-full level at j
 };
 
-// Fill the tile geometry for positions j in [tb, tb + kBuildTile).
-// D_j = max of lam over the B + 1 windows [i, i + B] that contain j; the
-// maximum over B + 1 consecutive values comes from a sparse table: the
-// maxima of runs of 2^s values by doubling, then two overlapping runs.
 // The tile's keys (with the halos) into shared memory, every load issued
 // before the first store; no barrier.
 constexpr int kKeyLoads = (kBuildTile + 2 * kHalo + 2 + kBuildThreads - 1) / kBuildThreads;
@@ -99,17 +95,13 @@ __device__ __forceinline__ void load_keys(TileGeom &g, const unsigned long long 
   }
 }
 
-// The rest of the geometry once the keys are in place (the first barrier
-// publishes them).
-__device__ void finish_geom(TileGeom &g, long long n, long long tb, int B, int bits);
-
+// Fill the tile geometry for positions j in [tb, tb + kBuildTile).
+// D_j = max of lam over the B + 1 windows [i, i + B] that contain j; the
+// maximum over B + 1 consecutive values comes from a sparse table: the
+// maxima of runs of 2^s values by doubling, then two overlapping runs.
 __device__ void load_geom(TileGeom &g, const unsigned long long *skeys,
                           long long n, long long tb, int B, int bits) {
   load_keys(g, skeys, n, tb, B);
-  finish_geom(g, n, tb, B, bits);
-}
-
-__device__ void finish_geom(TileGeom &g, long long n, long long tb, int B, int bits) {
   const long long k0 = tb - B - 1;
   __syncthreads();
   // lam[y] for i = k0 + y, y in [0, kBuildTile + B + 1)
@@ -268,7 +260,8 @@ __device__ __forceinline__ void thread_moments(const float4 *__restrict__ spm, l
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBuildThreads)
 build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
-                   int B, int bits, unsigned int *tile_counts, int ntiles) {
+                   int B, int bits, unsigned int *tile_counts, int ntiles,
+                   signed char *__restrict__ facts) {
   __shared__ TileGeom g;
   __shared__ unsigned s_cnt[kMaxLevels];
   const long long tb = (long long)blockIdx.x * kBuildTile;
@@ -280,6 +273,8 @@ build_count_kernel(const unsigned long long *__restrict__ skeys, long long n,
     long long j = tb + it * kBuildThreads + threadIdx.x;
     int s, L, e, Lp;
     position_facts(g, n, tb, j, B, bits, s, L, e, Lp);
+    // the write pass takes (s, L) from here instead of the keys
+    if (j < n) reinterpret_cast<char2 *>(facts)[j] = make_char2((signed char)s, (signed char)L);
     // only the levels some position of this warp starts a cell at
     const int lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(s <= L ? s : bits + 1));
     const int hi = __reduce_max_sync(0xffffffffu, L < 0 ? 0 : L);
@@ -371,13 +366,12 @@ constexpr size_t kWriteDynSmem = sizeof(long long) * 4 * kBuildTile;
 // (the tile's own prefix is added by the centre-of-mass pass), and the
 // tile's moment sums to tile_q[4 tile ..].
 __global__ void __launch_bounds__(kBuildThreads, 4)
-build_write_kernel(const unsigned long long *__restrict__ skeys,
+build_write_kernel(const signed char *__restrict__ facts,
                    const float4 *__restrict__ spm, long long n,
                    int B, int bits, const unsigned int *__restrict__ tile_off,
                    long long *tile_q, int ntiles, DevCtrl *ctrl, int4 *topo,
                    int *parent, unsigned char *level, int *arrive, long long *pq,
                    long long cap_nodes) {
-  __shared__ TileGeom g;
   __shared__ unsigned s_cnt[kBuildIters][kLvWarps][kMaxLevels];
   __shared__ long long s_base[kMaxLevels + 1];
   __shared__ long long s_wq[kBuildThreads / 32][4];
@@ -386,8 +380,19 @@ build_write_kernel(const unsigned long long *__restrict__ skeys,
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int tile = blockIdx.x;
   const long long tb = (long long)tile * kBuildTile;
-  // the tile's keys go to shared memory while the particles load
-  load_keys(g, skeys, n, tb, B);
+  // per position j, as the count pass found them: the first level at which
+  // j starts a cell and its leaf level, and the leaf level at j - 1; loaded
+  // with the particles, packed one byte each until the moments are done
+  unsigned packed[kBuildIters];
+#pragma unroll
+  for (int it = 0; it < kBuildIters; ++it) {
+    const long long j = tb + it * kBuildThreads + threadIdx.x;
+    unsigned sl = 0xffffu & (unsigned)((bits + 1) | (0xff << 8));   // s = bits + 1, L = -1
+    unsigned lp = 0xffu;                                            // Lp = -1
+    if (j < n) sl = __ldg(reinterpret_cast<const unsigned short *>(facts) + j);
+    if (j >= 1 && j <= n) lp = (unsigned char)__ldg(facts + 2 * (j - 1) + 1);
+    packed[it] = sl | (lp << 16);
+  }
   // the tile's moments: local exclusive prefix at positions
   // tb + kQPer * threadIdx.x + u, and the tile's sums
   {
@@ -448,14 +453,24 @@ build_write_kernel(const unsigned long long *__restrict__ skeys,
   }
   for (int k = threadIdx.x; k < kBuildIters * kLvWarps * kMaxLevels; k += blockDim.x)
     (&s_cnt[0][0][0])[k] = 0u;
-  finish_geom(g, n, tb, B, bits);            // synchronises the block
+  __syncthreads();                           // counts zeroed, bases set
   if (!s_ok) return;
-  // phase A: per (iteration, warp, level) counts, over the warp's levels only
+  // s: first level at which j starts a cell, L: its leaf level; e: the cells
+  // of levels above e that hold j - 1 end at j (lcp(key j-1, key j) = s - 1;
+  // -1 at j = n), Lp: the leaf level at j - 1; out of range nothing starts
+  // or ends
   int s[kBuildIters], L[kBuildIters], e[kBuildIters], Lp[kBuildIters];
 #pragma unroll
   for (int it = 0; it < kBuildIters; ++it) {
-    long long j = tb + it * kBuildThreads + threadIdx.x;
-    position_facts(g, n, tb, j, B, bits, s[it], L[it], e[it], Lp[it]);
+    const long long j = tb + it * kBuildThreads + threadIdx.x;
+    s[it] = (signed char)(packed[it] & 0xffu);
+    L[it] = (signed char)((packed[it] >> 8) & 0xffu);
+    Lp[it] = (signed char)((packed[it] >> 16) & 0xffu);
+    e[it] = (j >= 1 && j < n) ? s[it] - 1 : (j == n ? -1 : bits + 1);
+  }
+  // phase A: per (iteration, warp, level) counts, over the warp's levels only
+#pragma unroll
+  for (int it = 0; it < kBuildIters; ++it) {
     const int lo = (int)__reduce_min_sync(0xffffffffu, (unsigned)(s[it] <= L[it] ? s[it] : bits + 1));
     const int hi = __reduce_max_sync(0xffffffffu, L[it] < 0 ? 0 : L[it]);
     for (int l = lo; l <= hi; ++l) {
@@ -705,7 +720,7 @@ cudaError_t launch_build(const unsigned long long *skeys, const float4 *spm,
   if (opted < 0) return cudaErrorInvalidValue;
   {
     const cudaError_t le = launch_k(build_count_kernel, dim3((unsigned)ntiles), dim3(kBuildThreads), 0, s,
-      skeys, n, leaf_cap, bits, b.tile_counts, (int)ntiles);
+      skeys, n, leaf_cap, bits, b.tile_counts, (int)ntiles, b.facts);
     if (le != cudaSuccess) return le;
   }
   {
@@ -715,7 +730,7 @@ cudaError_t launch_build(const unsigned long long *skeys, const float4 *spm,
   }
   {
     const cudaError_t le = launch_k(build_write_kernel, dim3((unsigned)ntiles), dim3(kBuildThreads), kWriteDynSmem, s,
-      skeys, spm, n, leaf_cap, bits, b.tile_counts, b.tile_q, (int)ntiles, ctrl,
+      b.facts, spm, n, leaf_cap, bits, b.tile_counts, b.tile_q, (int)ntiles, ctrl,
       b.topo, b.parent, b.level, b.arrive, b.pq, b.cap_nodes);
     if (le != cudaSuccess) return le;
   }
