@@ -14,10 +14,12 @@
 //             (one past the common-prefix length with key j-1) and the level
 //             of its leaf (one past the deepest level whose cell holds more
 //             than B keys, found from lcp(key_i, key_{i+B}) over the B+1
-//             windows containing j).  Warp ballots count, per tile and per
-//             level, how many cells start in the tile.
+//             windows containing j), stored for the write pass.  Warp
+//             ballots count, per tile and per level, how many cells start in
+//             the tile.
 //   scan   -- one block per level turns the tile counts into tile offsets.
-//   write  -- the same ballots give each cell its breadth-first index
+//   write  -- from the stored levels (no keys needed), the same ballots
+//             give each cell its breadth-first index
 //             (level offset + rank among the level's cells in key order).
 //             The thread at a cell's first key writes (first, level, first
 //             child, parent); the thread at the position just past its last
